@@ -1,0 +1,212 @@
+/*
+ * mxq.h -- C ABI of libmxq, the MX-scaled FP8 output projection ("wo_a")
+ * for GB300 (sm_103a).
+ *
+ * The operator comes from the page "[ROCm][DSV4][Perf] Use FP8 WO_A output
+ * projection" (vLLM pull request 54894), Summary items 1-2: inverse RoPE
+ * fused with per-token E8M0 group quantisation of the attention output, then
+ * a batched a8w8 GEMM with MX (E8M0) scales against the checkpoint's native
+ * FP8 weight.  The unaligned-K linear and the load-time dequantiser come from
+ * "[ROCm][DSv4.1][Perf] Dequantize the MXFP8 weight once when dot_scaled
+ * cannot be used" (pull request 56560), Purpose.
+ *
+ * Conventions for every entry point:
+ *  - Pointers are device pointers unless stated otherwise.  The caller
+ *    allocates and owns every buffer; the library allocates no device memory
+ *    and keeps no per-tensor state (it caches only per-device properties).
+ *  - All layouts are row-major and contiguous.  "E4M3" is the OCP e4m3fn
+ *    byte (bias 7, max 448, S.1111.111 = NaN, no infinity).  "E8M0" is a
+ *    biased exponent byte: value 2^(byte-127), 0xFF = NaN.  BF16 is
+ *    bfloat16.  Scales come one per 128 consecutive elements along the
+ *    contraction axis; KG = ceil(K/128) and the last group may be partial.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream).  No call synchronises the host.
+ *  - Argument errors are detected on the host before anything is enqueued;
+ *    the call then returns the status and launches nothing.  The text of
+ *    the last error of the calling thread is available from
+ *    mxq_last_error().
+ *  - Every device pointer must be 16-byte aligned (MXQ_ERR_ALIGN).
+ *  - The device must be compute capability 10.3 (GB300); there is no
+ *    fallback path (MXQ_ERR_ARCH).
+ */
+#ifndef MXQ_H
+#define MXQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, passed as an opaque pointer so that this header needs no
+ * CUDA headers. */
+typedef void* mxq_stream_t;
+
+typedef enum mxq_status {
+  MXQ_OK = 0,
+  MXQ_ERR_NULL = 1,        /* a required pointer is NULL */
+  MXQ_ERR_SHAPE = 2,       /* a size is negative, too large or inconsistent */
+  MXQ_ERR_ALIGN = 3,       /* a pointer or leading dimension is misaligned */
+  MXQ_ERR_UNSUPPORTED = 4, /* a valid combination this library does not implement */
+  MXQ_ERR_ARCH = 5,        /* the current device is not sm_103 */
+  MXQ_ERR_WORKSPACE = 6,   /* workspace missing or smaller than required */
+  MXQ_ERR_CUDA = 7         /* a CUDA runtime/driver call failed */
+} mxq_status;
+
+/* Bits that kernels OR into a caller-provided int32 error word (err_flag).
+ * Data errors never trap: the affected output is written as described at
+ * each entry point and the bit is set. */
+#define MXQ_DEVERR_POSITION 0x1  /* a position outside [0, max_pos) */
+#define MXQ_DEVERR_SCALE 0x2     /* an FP32 scale that is not a power of two in range */
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* mxq_status_string(int status);
+
+/* Detail text of the last error returned to the calling thread ("" if none). */
+const char* mxq_last_error(void);
+
+/* Library ABI version: major*10000 + minor*100 + patch. */
+int mxq_version(void);
+
+/* 1 if the kernels of this library run on a device of compute capability
+ * major.minor (only 10.3, GB300), else 0.  Every entry point that launches
+ * work returns MXQ_ERR_ARCH on any other device. */
+int mxq_arch_supported(int major, int minor);
+
+/*
+ * Fused inverse RoPE + group-128 E8M0/E4M3 quantisation of the attention
+ * output.  FP8 WO_A page, Summary item 1 (the inverse rotation and the
+ * per-token E8M0 group quantisation run as one kernel) and Implementation
+ * (the model keeps BF16 cos/sin tables, made contiguous once at load).
+ *
+ *  x_bf16   [T, G, D] BF16.  Each of the T*G rows is one token's slice for
+ *           one output group.
+ *  pos      [T] int64 token positions.  Unused when R == 0 (may be NULL).
+ *  cos_bf16, sin_bf16
+ *           BF16 tables holding cos(p*theta_i) and sin(p*theta_i) of the
+ *           forward rotation: row p at element offset p*cs_ld, entries
+ *           i = 0..R/2-1.  cs_ld >= R/2, cs_ld % 8 == 0.  Unused when R == 0.
+ *  max_pos  number of table rows.
+ *  R        width of the rotated slice: the last R elements of each row,
+ *           rotate-half pairs (D-R+i, D-R/2+i), i < R/2.  For c = cos[p][i],
+ *           s = sin[p][i], the pair becomes
+ *             y0 = fl32(x0*c + x1*s),  y1 = fl32(x1*c - x0*s)
+ *           (rotation by -p*theta_i; each product is exact in fp32, so each
+ *           output is one rounding).  R must be 0 or a multiple of 16 with
+ *           R <= 128, and when R > 0, D % 128 == 0 (the slice lies in the
+ *           last scale group).
+ *  q_e4m3   [T, G, D] E4M3 codes out.
+ *  q_e8m0   [T, G, ceil(D/128)] E8M0 scale bytes out.
+ *  err_flag optional int32 device word; MXQ_DEVERR_POSITION is OR-ed in for a
+ *           token whose position is outside [0, max_pos), and that token's
+ *           codes and scale bytes are written as zeros.
+ *
+ * Per group (amax over the fp32 rotated values present in the group):
+ *   e = smallest integer with amax <= 448 * 2^e, clamped to [-127, 127]
+ *       (amax == 0 gives -127); scale byte = e + 127;
+ *   code = E4M3 round-to-nearest-even, saturating, of y * 2^-e.
+ * D % 16 == 0, D >= 16.  T == 0 is a no-op.
+ */
+int mxq_inv_rope_group_quant(const void* x_bf16, int64_t T, int32_t G, int32_t D, int32_t R,
+                             const int64_t* pos, const void* cos_bf16, const void* sin_bf16,
+                             int64_t cs_ld, int64_t max_pos, uint8_t* q_e4m3, uint8_t* q_e8m0,
+                             int32_t* err_flag, mxq_stream_t stream);
+
+/*
+ * Size in bytes of the prepared weight-scale buffer for B weight matrices
+ * of N rows and K columns.  Returns 0 for invalid sizes.
+ */
+size_t mxq_weight_scale_bytes(int32_t B, int32_t N, int32_t K);
+
+/*
+ * Load-time weight-scale layout transform.  FP8 WO_A page, Implementation
+ * (the group-128 weight and scale layouts are checked once, at load, before
+ * the FP8 path is used).  Input: w_e8m0 [B, N, ceil(K/128)] E8M0 bytes (one per weight row
+ * per 128-column group).  Output: w_sf_prepared, mxq_weight_scale_bytes()
+ * bytes, the layout the block-scaled GEMM reads: for each (b, group kg,
+ * block of 128 rows) a 512-byte atom in which row r = 32*j + i of the block
+ * owns the 32-bit word at byte offset 16*i + 4*j, holding the scale byte
+ * replicated into all four bytes.  Rows are padded to a multiple of 256
+ * with byte 127 (scale 1.0).  Run once after weight loading.
+ */
+int mxq_prepare_weight_scales(const uint8_t* w_e8m0, int32_t B, int32_t N, int32_t K,
+                              uint8_t* w_sf_prepared, mxq_stream_t stream);
+
+/* Workspace bytes mxq_bmm_a8w8 needs for these sizes (currently 0). */
+size_t mxq_bmm_workspace_bytes(int64_t T, int32_t G, int32_t N, int32_t K);
+
+/*
+ * Block-scaled batched a8w8 GEMM.  FP8 WO_A page, Summary item 2 (the GEMM
+ * reads the quantised activation and the weight exactly as the checkpoint
+ * stores it, FP8 codes plus MX scales), with K % 128 != 0 allowed (dequantise-once page, Purpose: K = 576, 288).
+ *
+ *  a_e4m3    [T, G, K] activation codes; a_e8m0 [T, G, ceil(K/128)] bytes
+ *            (exactly what mxq_inv_rope_group_quant writes).
+ *  w_e4m3    [G, N, K] weight codes; w_sf_prepared from
+ *            mxq_prepare_weight_scales(.., B=G, N, K).
+ *  out_bf16  [T, G, N]:  out[t,g,n] = bf16_rne( sum_k A[t,g,k] * W[g,n,k] )
+ *            with A = code * 2^(byte-127) per 128-group, likewise W; the sum
+ *            is accumulated in fp32 on the tensor cores.
+ *  ws        workspace of mxq_bmm_workspace_bytes() bytes (may be NULL if 0).
+ * Requirements: K % 16 == 0, N % 16 == 0, K <= 65536, G >= 1.  T == 0 is a
+ * no-op.
+ */
+int mxq_bmm_a8w8(const uint8_t* a_e4m3, const uint8_t* a_e8m0, const uint8_t* w_e4m3,
+                 const uint8_t* w_sf_prepared, void* out_bf16, int64_t T, int32_t G, int32_t N,
+                 int32_t K, void* ws, size_t ws_bytes, mxq_stream_t stream);
+
+/* Workspace bytes mxq_linear needs: the quantised activation codes and
+ * scales plus the GEMM workspace. */
+size_t mxq_linear_workspace_bytes(int64_t M, int32_t N, int32_t K);
+
+/*
+ * MXFP8 linear layer out[M, N] = x[M, K] * W[N, K]^T for any K % 16 == 0,
+ * including K % 128 != 0, with no per-call weight dequantisation
+ * (dequantise-once page, Purpose: K = 576 at TP4, 288 at TP8).  x is BF16;
+ * it is quantised per row in groups of 128 exactly as
+ * mxq_inv_rope_group_quant with R = 0, into the workspace, then multiplied
+ * by mxq_bmm_a8w8 with G = 1.  w_sf_prepared from
+ * mxq_prepare_weight_scales(.., B=1, N, K).  M == 0 is a no-op.
+ */
+int mxq_linear(const void* x_bf16, const uint8_t* w_e4m3, const uint8_t* w_sf_prepared,
+               void* out_bf16, int64_t M, int32_t N, int32_t K, void* ws, size_t ws_bytes,
+               mxq_stream_t stream);
+
+/*
+ * One-shot MXFP8 -> BF16 weight dequantisation.  Dequantise-once page,
+ * Purpose and "Why it is worth a patch" (the BF16 weight is built once at
+ * load; there it took six pointwise kernels and an FP32 intermediate, here
+ * it is a single pass).  w_e4m3 [B, N, K], w_e8m0 [B, N, ceil(K/128)];
+ * out_bf16[b,n,k] = bf16_rne(E4M3(code) * 2^(byte-127)) (NaN code or byte
+ * 0xFF gives NaN; overflow gives +-inf).  K % 16 == 0.
+ */
+int mxq_dequant_bf16(const uint8_t* w_e4m3, const uint8_t* w_e8m0, void* out_bf16, int32_t B,
+                     int32_t N, int32_t K, mxq_stream_t stream);
+
+/*
+ * Lossless FP32 power-of-two scales -> E8M0 bytes.  FP8 WO_A page,
+ * Implementation (checkpoints may carry FP32 scales that are exact powers of
+ * two; their exponent becomes the biased byte); functional-fixes page,
+ * Purpose (the conversion must not rely on FP8 arithmetic, so it is done by
+ * bit inspection).  s [n] float32 -> out [n] bytes:
+ * 2^k with -127 <= k <= 127 gives k + 127; any other value (zero, negative,
+ * not a power of two, out of range, inf, NaN) gives 0xFF and ORs
+ * MXQ_DEVERR_SCALE into *err_flag (if err_flag is not NULL).
+ */
+int mxq_scales_f32_to_e8m0(const float* s, int64_t n, uint8_t* out, int32_t* err_flag,
+                           mxq_stream_t stream);
+
+/*
+ * Watchdog word of the GEMM kernels on the current device (host call,
+ * synchronous).  Every wait inside a kernel is bounded; a wait that runs out
+ * sets a bit here and the kernel returns early instead of hanging.  0 means
+ * no wait ever ran out.  With clear != 0 the word is reset after reading.
+ */
+int mxq_watchdog_read(uint32_t* host_value, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXQ_H */

@@ -1,0 +1,223 @@
+"""Python binding of libmxq (the MX-scaled FP8 ``wo_a`` path for GB300).
+
+Argument marshalling only: every function here checks nothing that the C
+ABI does not check itself, allocates output tensors with torch when the
+caller passes none, and forwards raw device pointers plus the current
+torch CUDA stream to the entry point of the same name in ``libmxq.so``.
+All arithmetic runs in the library's CUDA kernels; there is no other path.
+A missing or unbuilt library raises ``MxqLibraryError`` on first use.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "MxqError", "MxqLibraryError", "lib", "library_path",
+    "mxq_inv_rope_group_quant", "mxq_weight_scale_bytes", "mxq_prepare_weight_scales",
+    "mxq_bmm_workspace_bytes", "mxq_bmm_a8w8", "mxq_linear_workspace_bytes", "mxq_linear",
+    "mxq_dequant_bf16", "mxq_scales_f32_to_e8m0", "mxq_watchdog_read", "mxq_arch_supported",
+    "mxq_version", "wo_a",
+]
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(HERE, "libmxq.so")
+
+MXQ_DEVERR_POSITION = 0x1
+MXQ_DEVERR_SCALE = 0x2
+
+
+class MxqLibraryError(RuntimeError):
+    """libmxq.so is missing or cannot be loaded."""
+
+
+class MxqError(RuntimeError):
+    def __init__(self, fn, status, detail):
+        self.status = status
+        super().__init__(f"{fn}: {_status_name(status)}: {detail}")
+
+
+_lib = None
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+_sz = ctypes.c_size_t
+
+_SIGNATURES = {
+    "mxq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "mxq_last_error": (ctypes.c_char_p, []),
+    "mxq_version": (ctypes.c_int, []),
+    "mxq_arch_supported": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
+    "mxq_inv_rope_group_quant": (ctypes.c_int, [_vp, _i64, _i32, _i32, _i32, _vp, _vp, _vp, _i64,
+                                                _i64, _vp, _vp, _vp, _vp]),
+    "mxq_weight_scale_bytes": (_sz, [_i32, _i32, _i32]),
+    "mxq_prepare_weight_scales": (ctypes.c_int, [_vp, _i32, _i32, _i32, _vp, _vp]),
+    "mxq_bmm_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32]),
+    "mxq_bmm_a8w8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _vp, _sz, _vp]),
+    "mxq_linear_workspace_bytes": (_sz, [_i64, _i32, _i32]),
+    "mxq_linear": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp, _sz, _vp]),
+    "mxq_dequant_bf16": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _vp]),
+    "mxq_scales_f32_to_e8m0": (ctypes.c_int, [_vp, _i64, _vp, _vp, _vp]),
+    "mxq_watchdog_read": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
+}
+
+
+def lib():
+    """The loaded ctypes library (loaded once)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise MxqLibraryError(
+                f"{library_path} not found; build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` or "
+                "`python mxfp8_block_scaled_inv_gb300/build.py`")
+        try:
+            handle = ctypes.CDLL(library_path)
+        except OSError as e:
+            raise MxqLibraryError(f"cannot load {library_path}: {e}") from e
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _status_name(status):
+    try:
+        return lib().mxq_status_string(status).decode()
+    except MxqLibraryError:
+        return str(status)
+
+
+def _check(fn, status):
+    if status != 0:
+        raise MxqError(fn, status, lib().mxq_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def mxq_version():
+    return lib().mxq_version()
+
+
+def mxq_arch_supported(major, minor):
+    return bool(lib().mxq_arch_supported(major, minor))
+
+
+def mxq_inv_rope_group_quant(x, pos=None, cos=None, sin=None, R=0, q=None, sc=None,
+                             err_flag=None, stream=None):
+    """x bf16 [T, G, D] -> (codes uint8 [T, G, D], scales uint8 [T, G, ceil(D/128)]).
+
+    cos/sin: bf16 [max_pos, >= R/2] (row stride = cos.stride(0)); pos int64 [T]."""
+    T, G, D = x.shape
+    KG = (D + 127) // 128
+    if q is None:
+        q = torch.empty((T, G, D), dtype=torch.uint8, device=x.device)
+    if sc is None:
+        sc = torch.empty((T, G, KG), dtype=torch.uint8, device=x.device)
+    cs_ld = cos.stride(0) if cos is not None else 0
+    max_pos = cos.shape[0] if cos is not None else 0
+    st = lib().mxq_inv_rope_group_quant(_ptr(x), T, G, D, R, _ptr(pos), _ptr(cos), _ptr(sin),
+                                        cs_ld, max_pos, _ptr(q), _ptr(sc), _ptr(err_flag),
+                                        _stream(stream))
+    _check("mxq_inv_rope_group_quant", st)
+    return q, sc
+
+
+def mxq_weight_scale_bytes(B, N, K):
+    return lib().mxq_weight_scale_bytes(B, N, K)
+
+
+def mxq_prepare_weight_scales(w_e8m0, K, out=None, stream=None):
+    """w_e8m0 uint8 [B, N, ceil(K/128)] -> prepared scale bytes for mxq_bmm_a8w8."""
+    B, N, _ = w_e8m0.shape
+    if out is None:
+        out = torch.empty(mxq_weight_scale_bytes(B, N, K), dtype=torch.uint8, device=w_e8m0.device)
+    st = lib().mxq_prepare_weight_scales(_ptr(w_e8m0), B, N, K, _ptr(out), _stream(stream))
+    _check("mxq_prepare_weight_scales", st)
+    return out
+
+
+def mxq_bmm_workspace_bytes(T, G, N, K):
+    return lib().mxq_bmm_workspace_bytes(T, G, N, K)
+
+
+def mxq_bmm_a8w8(a, a_sf, w, w_sf, out=None, ws=None, stream=None):
+    """a uint8 [T, G, K], a_sf uint8 [T, G, KG], w uint8 [G, N, K], w_sf prepared
+    -> out bf16 [T, G, N]."""
+    T, G, K = a.shape
+    N = w.shape[1]
+    if out is None:
+        out = torch.empty((T, G, N), dtype=torch.bfloat16, device=a.device)
+    need = mxq_bmm_workspace_bytes(T, G, N, K)
+    if ws is None and need > 0:
+        ws = torch.empty(need, dtype=torch.uint8, device=a.device)
+    st = lib().mxq_bmm_a8w8(_ptr(a), _ptr(a_sf), _ptr(w), _ptr(w_sf), _ptr(out), T, G, N, K,
+                            _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream))
+    _check("mxq_bmm_a8w8", st)
+    return out
+
+
+def mxq_linear_workspace_bytes(M, N, K):
+    return lib().mxq_linear_workspace_bytes(M, N, K)
+
+
+def mxq_linear(x, w, w_sf, out=None, ws=None, stream=None):
+    """x bf16 [M, K], w uint8 [N, K], w_sf prepared (B=1) -> out bf16 [M, N]."""
+    M, K = x.shape
+    N = w.shape[-2]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = torch.empty(max(mxq_linear_workspace_bytes(M, N, K), 16), dtype=torch.uint8,
+                         device=x.device)
+    st = lib().mxq_linear(_ptr(x), _ptr(w), _ptr(w_sf), _ptr(out), M, N, K, _ptr(ws), ws.numel(),
+                          _stream(stream))
+    _check("mxq_linear", st)
+    return out
+
+
+def mxq_dequant_bf16(w, w_e8m0, out=None, stream=None):
+    """w uint8 [B, N, K], w_e8m0 uint8 [B, N, ceil(K/128)] -> bf16 [B, N, K]."""
+    B, N, K = w.shape
+    if out is None:
+        out = torch.empty((B, N, K), dtype=torch.bfloat16, device=w.device)
+    st = lib().mxq_dequant_bf16(_ptr(w), _ptr(w_e8m0), _ptr(out), B, N, K, _stream(stream))
+    _check("mxq_dequant_bf16", st)
+    return out
+
+
+def mxq_scales_f32_to_e8m0(s, out=None, err_flag=None, stream=None):
+    n = s.numel()
+    if out is None:
+        out = torch.empty(s.shape, dtype=torch.uint8, device=s.device)
+    st = lib().mxq_scales_f32_to_e8m0(_ptr(s), n, _ptr(out), _ptr(err_flag), _stream(stream))
+    _check("mxq_scales_f32_to_e8m0", st)
+    return out
+
+
+def mxq_watchdog_read(clear=False):
+    v = ctypes.c_uint32(0)
+    _check("mxq_watchdog_read", lib().mxq_watchdog_read(ctypes.byref(v), 1 if clear else 0))
+    return v.value
+
+
+def wo_a(x, pos, cos, sin, w, w_sf, R=64, out=None, codes=None, scales=None, err_flag=None,
+         stream=None):
+    """The fused wo_a projection as two library calls on one stream:
+    inverse RoPE + group quantisation, then the block-scaled batched GEMM."""
+    q, sc = mxq_inv_rope_group_quant(x, pos, cos, sin, R, q=codes, sc=scales,
+                                     err_flag=err_flag, stream=stream)
+    return mxq_bmm_a8w8(q, sc, w, w_sf, out=out, stream=stream)

@@ -1,0 +1,43 @@
+// Internal declarations shared by the C-ABI layer (api.cpp) and the kernel
+// translation units.  Launchers assume their arguments were validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mxq {
+
+constexpr int kGroup = 128;        // scale-group width along the contraction axis
+constexpr int kSfAtomBytes = 512;  // one 128-row x 4-byte scale-factor atom
+constexpr int kSfRowPad = 256;     // prepared weight-scale rows are padded to this
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Number of 128-row atoms per (b, kg) in the prepared weight-scale layout.
+inline int64_t sf_row_blocks(int64_t N) { return ceil_div(N, kSfRowPad) * (kSfRowPad / 128); }
+
+cudaError_t launch_inv_rope_group_quant(const void* x, int64_t T, int G, int D, int R,
+                                        const int64_t* pos, const void* cos, const void* sin,
+                                        int64_t cs_ld, int64_t max_pos, uint8_t* q, uint8_t* sc,
+                                        int32_t* err_flag, int num_sms, cudaStream_t s);
+
+cudaError_t launch_prepare_weight_scales(const uint8_t* w_e8m0, int B, int N, int K, uint8_t* out,
+                                         cudaStream_t s);
+
+cudaError_t launch_dequant_bf16(const uint8_t* w, const uint8_t* sc, void* out, int B, int N, int K,
+                                int num_sms, cudaStream_t s);
+
+cudaError_t launch_scales_f32_to_e8m0(const float* s, int64_t n, uint8_t* out, int32_t* err_flag,
+                                      cudaStream_t st);
+
+// Block-scaled GEMM.  Returns cudaSuccess or the first CUDA error; a
+// non-CUDA failure (e.g. tensor-map encoding) is reported as
+// cudaErrorInvalidValue with detail text in *why.
+cudaError_t launch_bmm_a8w8(const uint8_t* a, const uint8_t* a_sf, const uint8_t* w,
+                            const uint8_t* w_sf, void* out, int64_t T, int G, int N, int K,
+                            int num_sms, cudaStream_t s, const char** why);
+
+cudaError_t watchdog_read(uint32_t* value, bool clear);
+
+}  // namespace mxq

@@ -8,19 +8,20 @@ CUDA library; the two meet only on the seeded inputs from ``workloads``.
 What it computes, and where each step comes from:
 
 * Page "[ROCm][DSV4][Perf] Use FP8 WO_A output projection", Summary items 1-2:
-  inverse RoPE fused with per-token E8M0 group quantisation of the attention
-  output, then a batched a8w8 GEMM against the checkpoint's native FP8 weight
-  with MX (E8M0) scales.  Implementation bullets: E8M0 scale bytes, or
-  positive power-of-two FP32 scales converted losslessly to biased exponent
-  bytes; group-128 layouts; cached BF16 cos/sin views.
+  the attention output is un-rotated (inverse RoPE) and quantised per token
+  in 128-wide groups with one E8M0 scale each, in one pass; a batched a8w8
+  GEMM then multiplies it by the FP8 weight as stored in the checkpoint,
+  codes plus MX scales.  Implementation section: scales come either as E8M0
+  bytes or as FP32 exact powers of two whose exponent becomes the byte; the
+  layouts are group-128; the cos/sin tables are BF16.
 * Page "[ROCm][DSv4] Functional fixes for DeepSeek V4 on MI300X/MI325X",
   Purpose: OCP E4M3 encoding (max 448) on the current architecture, scale
   conversion by bit manipulation rather than FP8 arithmetic.
 * Page "[ROCm][DSv4.1][Perf] Dequantize the MXFP8 weight once when
-  dot_scaled cannot be used", Purpose and "Why it is worth a patch":
-  ``w_bf16 = dequant_mxfp8_to_bf16(weight, weight_scale)`` (value = E4M3
-  code times 2^(scale byte - 127), rounded once to BF16), and the unaligned
-  K = 576 / 288 shapes.
+  dot_scaled cannot be used", Purpose and "Why it is worth a patch": the
+  BF16 copy of an MXFP8 weight is each decoded E4M3 value times
+  2^(scale byte - 127), rounded once to BF16; the unaligned shapes are
+  K = 576 and 288.
 
 Readings taken where the pages are silent (each one is listed in the design doc):
 
@@ -129,9 +130,9 @@ def e8m0_exponent(amax: np.ndarray) -> np.ndarray:
 
 # --------------------------------------------------------------------------
 # Inverse RoPE (fp32, fixed evaluation order).
-# FP8 WO_A page, Summary item 1 ("fuses inverse RoPE with per-token E8M0
-# group quantization") and Implementation ("cache contiguous BF16
-# cosine/sine cache views").
+# FP8 WO_A page, Summary item 1 (the inverse rotation runs inside the
+# quantisation kernel) and Implementation (BF16 cos/sin tables kept by the
+# model).
 # --------------------------------------------------------------------------
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     """Widen BF16 bit patterns (uint16) to float32; exact."""
@@ -200,9 +201,9 @@ def inv_rope_group_quant(x_bits: np.ndarray, pos: np.ndarray, cos_bits: np.ndarr
 
 # --------------------------------------------------------------------------
 # Dequantisation to BF16.
-# Dequantize-once page, Purpose: w_bf16 = dequant_mxfp8_to_bf16(weight,
-# weight_scale); the profile in Test Result shows it computed as exp2 of the
-# integer scale exponent times the decoded value.
+# Dequantize-once page, Purpose: the load-time BF16 weight; its Test Result
+# profile shows the value built as exp2 of the integer scale exponent times
+# the decoded code.
 # --------------------------------------------------------------------------
 def bf16_rne_bits(v: np.ndarray) -> np.ndarray:
     """Round float64 values to BF16 (round to nearest, ties to even), with
@@ -291,9 +292,9 @@ def gemm_tolerance(y_ref, S):
 
 # --------------------------------------------------------------------------
 # FP32 power-of-two scales -> E8M0 bytes.
-# FP8 WO_A page, Implementation: "losslessly convert positive power-of-two
-# FP32 scales to biased E8M0 exponent bytes"; functional-fixes page: do the
-# conversion without FP8 arithmetic.
+# FP8 WO_A page, Implementation: an FP32 scale that is an exact positive power
+# of two carries no information beyond its exponent, so it maps losslessly to
+# the biased byte; functional-fixes page: no FP8 arithmetic in the conversion.
 # --------------------------------------------------------------------------
 def scales_f32_to_e8m0(s: np.ndarray):
     """Returns (bytes uint8, ok bool).  A value is accepted when it is a

@@ -1,0 +1,138 @@
+"""The C ABI without a GPU: the library loads, exports every entry point the
+header declares, and rejects invalid arguments on the host (returning the
+documented status and launching nothing)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "mxq.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from mxfp8_block_scaled_inv_gb300 import build as B
+
+    B.build()
+    import mxfp8_block_scaled_inv_gb300 as mxq
+
+    return mxq.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mxq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ["mxq_inv_rope_group_quant", "mxq_bmm_a8w8", "mxq_linear", "mxq_dequant_bf16",
+              "mxq_prepare_weight_scales", "mxq_scales_f32_to_e8m0"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+
+
+def test_status_strings_and_version(L):
+    assert L.mxq_status_string(0) == b"MXQ_OK"
+    assert L.mxq_status_string(5) == b"MXQ_ERR_ARCH"
+    assert L.mxq_status_string(99) == b"MXQ_ERR_UNKNOWN"
+    assert L.mxq_version() >= 100
+
+
+def test_arch_gate(L):
+    assert L.mxq_arch_supported(10, 3) == 1
+    for mm in [(10, 0), (10, 1), (9, 0), (12, 0), (8, 9)]:
+        assert L.mxq_arch_supported(*mm) == 0
+
+
+P = ctypes.c_void_p(1 << 20)     # 16-byte aligned fake device address (never dereferenced)
+U = ctypes.c_void_p((1 << 20) + 8)  # misaligned
+
+
+def quant(L, x=P, T=4, G=1, D=256, R=0, pos=P, cos=P, sin=P, cs_ld=32, max_pos=16, q=P, sc=P,
+          err=None):
+    return L.mxq_inv_rope_group_quant(x, T, G, D, R, pos, cos, sin, cs_ld, max_pos, q, sc, err, None)
+
+
+def test_quant_argument_errors(L):
+    assert quant(L, x=None) == 1
+    assert quant(L, q=None) == 1
+    assert quant(L, T=-1) == 2
+    assert quant(L, G=0) == 2
+    assert quant(L, D=8) == 2
+    assert quant(L, D=264) == 2                 # D % 16
+    assert quant(L, R=8, D=256) == 4            # R % 16
+    assert quant(L, R=144, D=256) == 4          # R > 128
+    assert quant(L, R=64, D=272) == 4           # RoPE needs D % 128 == 0
+    assert quant(L, R=64, cs_ld=16) == 2        # cs_ld < R/2
+    assert quant(L, R=64, cs_ld=36) == 3        # cs_ld % 8
+    assert quant(L, R=64, max_pos=0) == 2
+    assert quant(L, R=64, pos=None) == 1
+    assert quant(L, x=U) == 3
+    assert quant(L, R=64, cos=U) == 3
+    assert quant(L, err=ctypes.c_void_p((1 << 20) + 2)) == 3
+    assert quant(L, T=0, x=None, q=None, sc=None) == 0  # empty input is a no-op
+
+
+def bmm(L, a=P, asf=P, w=P, wsf=P, out=P, T=4, G=1, N=128, K=256, ws=None, ws_bytes=0):
+    return L.mxq_bmm_a8w8(a, asf, w, wsf, out, T, G, N, K, ws, ws_bytes, None)
+
+
+def test_bmm_argument_errors(L):
+    assert bmm(L, a=None) == 1
+    assert bmm(L, wsf=None) == 1
+    assert bmm(L, K=8) == 2
+    assert bmm(L, K=264) == 2
+    assert bmm(L, N=120) == 2
+    assert bmm(L, G=0) == 2
+    assert bmm(L, T=-3) == 2
+    assert bmm(L, K=65536 + 16) == 4
+    assert bmm(L, out=U) == 3
+    assert bmm(L, T=0, a=None, out=None) == 0
+    assert L.mxq_bmm_workspace_bytes(8192, 8, 1024, 4096) == 0
+
+
+def test_linear_argument_errors(L):
+    need = L.mxq_linear_workspace_bytes(8, 5120, 576)
+    assert need == 8 * 576 + 256 + 0  # codes (4608 B, 256-aligned) + 8*5 scale bytes -> 256
+    assert L.mxq_linear(P, P, P, P, 8, 5120, 576, None, 0, None) == 6
+    assert L.mxq_linear(P, P, P, P, 8, 5120, 576, P, need - 1, None) == 6
+    assert L.mxq_linear(None, P, P, P, 8, 5120, 576, P, need, None) == 1
+    assert L.mxq_linear(P, P, P, P, 8, 5120, 570, P, need, None) == 2
+    assert L.mxq_linear(P, P, P, P, 0, 5120, 576, None, 0, None) == 0
+
+
+def test_dequant_and_scale_argument_errors(L):
+    assert L.mxq_dequant_bf16(None, P, P, 1, 16, 128, None) == 1
+    assert L.mxq_dequant_bf16(P, P, P, 1, 16, 120, None) == 2
+    assert L.mxq_dequant_bf16(P, U, P, 1, 16, 128, None) == 3
+    assert L.mxq_dequant_bf16(P, P, P, 0, 16, 128, None) == 0
+    assert L.mxq_scales_f32_to_e8m0(None, 4, P, None, None) == 1
+    assert L.mxq_scales_f32_to_e8m0(P, -1, P, None, None) == 2
+    assert L.mxq_scales_f32_to_e8m0(P, 0, None, None, None) == 0
+    assert L.mxq_prepare_weight_scales(P, 1, 128, 100, P, None) == 2
+    assert L.mxq_prepare_weight_scales(None, 1, 128, 128, P, None) == 1
+
+
+def test_weight_scale_bytes(L):
+    # G * ceil(K/128) * (rows padded to 256)/128 * 512
+    assert L.mxq_weight_scale_bytes(8, 1024, 4096) == 8 * 32 * 8 * 512
+    assert L.mxq_weight_scale_bytes(1, 5120, 576) == 5 * 40 * 512
+    assert L.mxq_weight_scale_bytes(2, 128, 256) == 2 * 2 * 2 * 512
+    assert L.mxq_weight_scale_bytes(0, 128, 256) == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_valid_call_without_device_reports_cuda_error(L):
+    assert quant(L) == 7
+    assert bmm(L) == 7
