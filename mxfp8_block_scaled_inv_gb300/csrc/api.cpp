@@ -101,6 +101,7 @@ int mxq_inv_rope_group_quant(const void* x_bf16, int64_t T, int32_t G, int32_t D
     return fail(MXQ_ERR_SHAPE, "need T >= 0, G >= 1, D >= 16, R >= 0 (T=%lld G=%d D=%d R=%d)",
                 (long long)T, G, D, R);
   if (D % 16 != 0) return fail(MXQ_ERR_SHAPE, "D %% 16 != 0 (D=%d)", D);
+  if (T == 0) return ok();
   if (R > 0) {
     if (R % 16 != 0 || R > 128 || R > D)
       return fail(MXQ_ERR_UNSUPPORTED, "R must be a multiple of 16, <= 128 and <= D (R=%d)", R);
@@ -114,7 +115,6 @@ int mxq_inv_rope_group_quant(const void* x_bf16, int64_t T, int32_t G, int32_t D
     if (!aligned16(cos_bf16) || !aligned16(sin_bf16) || (reinterpret_cast<uintptr_t>(pos) & 7u))
       return fail(MXQ_ERR_ALIGN, "cos/sin must be 16-byte aligned and pos 8-byte aligned");
   }
-  if (T == 0) return ok();
   if (!x_bf16 || !q_e4m3 || !q_e8m0) return fail(MXQ_ERR_NULL, "x, q_e4m3 or q_e8m0 is NULL");
   if (!aligned16(x_bf16) || !aligned16(q_e4m3) || !aligned16(q_e8m0))
     return fail(MXQ_ERR_ALIGN, "x, q_e4m3 and q_e8m0 must be 16-byte aligned");

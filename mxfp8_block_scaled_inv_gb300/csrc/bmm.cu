@@ -37,6 +37,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "mxq.h"
@@ -389,9 +390,19 @@ cudaError_t launch_cfg(const uint8_t* a, const uint8_t* w, BmmArgs args, cudaStr
     return cudaErrorInvalidValue;
   }
   auto kern = bmm_a8w8_kernel<SWAP, BN, NSTAGE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_BYTES);
+  // The shared-memory opt-in is set once per device (a host-side call that
+  // must not run inside stream capture, so the first call on a device should
+  // happen before any capture).
+  static std::atomic<uint64_t> smem_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(smem_set.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    smem_set.fetch_or(bit, std::memory_order_acq_rel);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(args.x_tiles * args.y_tiles * args.splits), (unsigned)args.G, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
