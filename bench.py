@@ -75,6 +75,26 @@ def load_peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+def measured_traffic(key):
+    """DRAM bytes per launch from the committed ncu capture, or None when the
+    kernel source has changed since that capture."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            parts = dict(p.split("=", 1) for p in line.split()[1:] if "=" in p)
+            if line.split() and line.split()[0] == key:
+                src = os.path.join(ROOT, parts["source"])
+                with open(src, "rb") as g:
+                    if hashlib.sha256(g.read()).hexdigest()[:16] != parts["sha256_16"]:
+                        return None
+                return int(parts["bytes"])
+    return None
+
+
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -520,11 +540,7 @@ def main():
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
     gemm_tflops = gemm_flops(T_PREFILL) / (t_gemm * 1e-3) / 1e12
     quant_gbs = quant_bytes(T_PREFILL) / (t_quant * 1e-3) / 1e9
-    traffic = None
-    tf = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tf):
-        with open(tf) as f:
-            traffic = json.load(f).get("bmm_a8w8_prefill_bytes_per_launch")
+    traffic = measured_traffic("bmm_a8w8_prefill_8k")
 
     sec = {}
     if not args.no_secondary and rank == 0:
@@ -554,7 +570,8 @@ def main():
                                         f"{peaks['bf16_tflops_sustained']} TFLOP/s (fp8/bf16 nominal 4.5/2.25)"},
             "quantiser_roofline": {"bound": "hbm", "achieved": round(quant_gbs, 1),
                                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                   "frac": round(quant_gbs / peaks["hbm_gbs"], 4)},
+                                   "frac": round(quant_gbs / peaks["hbm_gbs"], 4),
+                                   "traffic": measured_traffic("inv_rope_group_quant_prefill_8k")},
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
             "clocks": clk,
