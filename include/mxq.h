@@ -197,6 +197,40 @@ int mxq_dequant_bf16(const uint8_t* w_e4m3, const uint8_t* w_e8m0, void* out_bf1
 int mxq_scales_f32_to_e8m0(const float* s, int64_t n, uint8_t* out, int32_t* err_flag,
                            mxq_stream_t stream);
 
+/* Size in bytes of the fixed device scratch array behind
+ * mxq_linear_noalloc (4 MiB). */
+#define MXQ_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
+
+/*
+ * mxq_linear without a workspace argument, for callers that cannot allocate
+ * device memory.  The pages have no counterpart of this entry point; it
+ * exists for users of this library.
+ *
+ * Who needs it: a host program that links only this C library and has no
+ * device allocator of its own to hand out a workspace, or a serving loop that
+ * must never call cudaMalloc/cudaFree (they can synchronise the device) and
+ * whose device memory was reserved up front by another component.
+ *
+ * Same operation, arguments and results as mxq_linear.  Instead of a
+ * caller-provided workspace it uses a fixed scratch array that the library
+ * keeps in the device memory of every GPU it is loaded on, until the process
+ * exits.  The call allocates nothing.
+ *  - Limit: the quantised activation must fit the array:
+ *    round_up(M*K, 256) + round_up(M*ceil(K/128), 256) <= MXQ_NOALLOC_SCRATCH_BYTES
+ *    (for example M <= 7219 rows at K = 576, 1806 at K = 2304); larger sizes return
+ *    MXQ_ERR_WORKSPACE and launch nothing.
+ *  - The first call on each device looks up the array's device address (a
+ *    host-side runtime query, done once per device with that device current);
+ *    make that first call before any stream capture.
+ *  - All calls on a device share the one array, and it keeps whatever the
+ *    last call left in it (every byte a call reads is first written by that
+ *    same call).  Calls whose kernels overlap on the GPU -- on different
+ *    streams, or from different host threads without ordering -- race on the
+ *    array and give wrong results: keep them ordered, e.g. on one stream.
+ */
+int mxq_linear_noalloc(const void* x_bf16, const uint8_t* w_e4m3, const uint8_t* w_sf_prepared,
+                       void* out_bf16, int64_t M, int32_t N, int32_t K, mxq_stream_t stream);
+
 /*
  * Watchdog word of the GEMM kernels on the current device (host call,
  * synchronous).  Every wait inside a kernel is bounded; a wait that runs out

@@ -19,6 +19,7 @@ __all__ = [
     "MxqError", "MxqLibraryError", "lib", "library_path",
     "mxq_inv_rope_group_quant", "mxq_weight_scale_bytes", "mxq_prepare_weight_scales",
     "mxq_bmm_workspace_bytes", "mxq_bmm_a8w8", "mxq_linear_workspace_bytes", "mxq_linear",
+    "mxq_linear_noalloc",
     "mxq_dequant_bf16", "mxq_scales_f32_to_e8m0", "mxq_watchdog_read", "mxq_arch_supported",
     "mxq_version", "wo_a",
 ]
@@ -62,6 +63,7 @@ _SIGNATURES = {
     "mxq_dequant_bf16": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _vp]),
     "mxq_scales_f32_to_e8m0": (ctypes.c_int, [_vp, _i64, _vp, _vp, _vp]),
     "mxq_watchdog_read": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
+    "mxq_linear_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp]),
 }
 
 
@@ -186,6 +188,19 @@ def mxq_linear(x, w, w_sf, out=None, ws=None, stream=None):
     st = lib().mxq_linear(_ptr(x), _ptr(w), _ptr(w_sf), _ptr(out), M, N, K, _ptr(ws), ws.numel(),
                           _stream(stream))
     _check("mxq_linear", st)
+    return out
+
+
+def mxq_linear_noalloc(x, w, w_sf, out=None, stream=None):
+    """mxq_linear with the library's fixed device scratch instead of a workspace
+    (for callers that cannot allocate; see include/mxq.h for the size limit and
+    the rule that overlapping calls race)."""
+    M, K = x.shape
+    N = w.shape[-2]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    st = lib().mxq_linear_noalloc(_ptr(x), _ptr(w), _ptr(w_sf), _ptr(out), M, N, K, _stream(stream))
+    _check("mxq_linear_noalloc", st)
     return out
 
 

@@ -71,6 +71,8 @@ size_t round256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 }  // namespace
 
+int mxq::set_error(int status, const char* text) { return fail(status, "%s", text); }
+
 extern "C" {
 
 const char* mxq_status_string(int status) {

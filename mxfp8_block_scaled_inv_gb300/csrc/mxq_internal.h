@@ -40,4 +40,8 @@ cudaError_t launch_bmm_a8w8(const uint8_t* a, const uint8_t* a_sf, const uint8_t
 
 cudaError_t watchdog_read(uint32_t* value, bool clear);
 
+// Stores `text` as the calling thread's last-error text (mxq_last_error) and
+// returns `status`.
+int set_error(int status, const char* text);
+
 }  // namespace mxq

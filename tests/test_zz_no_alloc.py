@@ -1,0 +1,76 @@
+"""mxq_linear_noalloc: the MXFP8 linear for callers that cannot allocate
+device memory (a plain-C host program with no device allocator of its own,
+or a serving loop that must not call cudaMalloc/cudaFree because they can
+synchronise the device).  It runs the same kernels as mxq_linear but takes
+its scratch from a fixed array inside the library.
+
+This file is collected last on purpose: the entry point shares one array
+per device across calls, so it is also exercised after every other test has
+run in the same process; it must pass both ways."""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from cases import oracle_weights, to_dev
+from oracle import mx_oracle as O
+
+
+@pytest.fixture(scope="module")
+def mxq():
+    import mxfp8_block_scaled_inv_gb300 as m
+    from mxfp8_block_scaled_inv_gb300 import build
+
+    build.build()
+    m.lib()
+    return m
+
+
+def _noalloc(mxq, x, w, wsf):
+    """Call the entry point through the C ABI (ctypes), on the current stream."""
+    M, K = x.shape
+    N = w.shape[0]
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    st = mxq.lib().mxq_linear_noalloc(
+        ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(wsf.data_ptr()),
+        ctypes.c_void_p(out.data_ptr()), M, N, K,
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, mxq.lib().mxq_last_error()
+    return out
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_linear_on_two_calls_in_a_row(mxq):
+    # Two different problems back to back: the second call reuses the array
+    # the first one filled (larger, then smaller), with other inputs.
+    for M, K, seed in [(8, 2304, 4100), (3, 576, 4200)]:
+        N = 5120
+        x = W.bf16_normal((M, K), seed=seed)
+        w, sw = oracle_weights(1, N, K, seed=seed + 1)
+        xd, wd, swd = to_dev(x, w[0], sw)
+        wsf = mxq.mxq_prepare_weight_scales(swd, K)
+        got = _noalloc(mxq, xd, wd, wsf)
+        ref = mxq.mxq_linear(xd, wd, wsf)
+        torch.cuda.synchronize()
+        # Tolerance of the GEMM parity tests, around the existing entry point's output.
+        _, S, _, _ = O.linear_ref(W.bf16_bits(x), w[0], sw[0])
+        g = got.float().cpu().numpy().astype(np.float64)
+        r = ref.float().cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(g - r) <= O.gemm_tolerance(r, S)), f"M={M} K={K}"
+
+
+def test_noalloc_rejects_sizes_beyond_the_scratch():
+    import mxfp8_block_scaled_inv_gb300 as m
+    from mxfp8_block_scaled_inv_gb300 import build
+
+    build.build()
+    L = m.lib()
+    p = ctypes.c_void_p(1 << 20)
+    # 7220 rows at K = 576 need 4,195,072 bytes > 4 MiB: rejected before any launch.
+    assert L.mxq_linear_noalloc(p, p, p, p, 7220, 5120, 576, None) == 6
+    assert b"scratch" in L.mxq_last_error()
+    assert L.mxq_linear_noalloc(p, p, p, p, 4, 5120, 570, None) == 2
+    assert L.mxq_linear_noalloc(p, p, p, p, 0, 5120, 576, None) == 0
