@@ -156,8 +156,9 @@ int mxq_bmm_a8w8(const uint8_t* a_e4m3, const uint8_t* a_e8m0, const uint8_t* w_
                  const uint8_t* w_sf_prepared, void* out_bf16, int64_t T, int32_t G, int32_t N,
                  int32_t K, void* ws, size_t ws_bytes, mxq_stream_t stream);
 
-/* Workspace bytes mxq_linear needs: the quantised activation codes and
- * scales plus the GEMM workspace. */
+/* Workspace bytes mxq_linear needs: 0 for M <= 64 (one fused launch),
+ * otherwise the quantised activation codes and scales plus the GEMM
+ * workspace. */
 size_t mxq_linear_workspace_bytes(int64_t M, int32_t N, int32_t K);
 
 /*
@@ -165,13 +166,35 @@ size_t mxq_linear_workspace_bytes(int64_t M, int32_t N, int32_t K);
  * including K % 128 != 0, with no per-call weight dequantisation
  * (dequantise-once page, Purpose: K = 576 at TP4, 288 at TP8).  x is BF16;
  * it is quantised per row in groups of 128 exactly as
- * mxq_inv_rope_group_quant with R = 0, into the workspace, then multiplied
- * by mxq_bmm_a8w8 with G = 1.  w_sf_prepared from
+ * mxq_inv_rope_group_quant with R = 0 and multiplied as mxq_bmm_a8w8 with
+ * G = 1: for M <= 64 in one launch that quantises inside the GEMM, else
+ * through the workspace.  w_sf_prepared from
  * mxq_prepare_weight_scales(.., B=1, N, K).  M == 0 is a no-op.
  */
 int mxq_linear(const void* x_bf16, const uint8_t* w_e4m3, const uint8_t* w_sf_prepared,
                void* out_bf16, int64_t M, int32_t N, int32_t K, void* ws, size_t ws_bytes,
                mxq_stream_t stream);
+
+/* Workspace bytes mxq_wo_a needs: 0 for T <= 64, else T*G*D code bytes and
+ * T*G*ceil(D/128) scale bytes (each rounded up to 256). */
+size_t mxq_wo_a_workspace_bytes(int64_t T, int32_t G, int32_t D, int32_t N);
+
+/*
+ * The whole wo_a projection in one call: mxq_inv_rope_group_quant of x
+ * followed by mxq_bmm_a8w8 against W, with the same arguments, layouts,
+ * rules and results (codes and scales bit-identical; the output equal to
+ * the two-call sequence).  FP8 WO_A page, Summary items 1-2.
+ *
+ * For T <= 64 tokens (decode) it is ONE launch: the GEMM reads the BF16 x
+ * and quantises each tile itself, so neither the codes nor a second launch
+ * cost anything (this goes beyond the pages' two-kernel design).  For larger
+ * T the codes go through `ws` (mxq_wo_a_workspace_bytes) and two kernels run.
+ * err_flag as in mxq_inv_rope_group_quant.  T == 0 is a no-op.
+ */
+int mxq_wo_a(const void* x_bf16, const int64_t* pos, const void* cos_bf16, const void* sin_bf16,
+             int64_t cs_ld, int64_t max_pos, const uint8_t* w_e4m3, const uint8_t* w_sf_prepared,
+             void* out_bf16, int64_t T, int32_t G, int32_t D, int32_t N, int32_t R,
+             int32_t* err_flag, void* ws, size_t ws_bytes, mxq_stream_t stream);
 
 /*
  * One-shot MXFP8 -> BF16 weight dequantisation.  Dequantise-once page,
@@ -238,6 +261,15 @@ int mxq_linear_noalloc(const void* x_bf16, const uint8_t* w_e4m3, const uint8_t*
  * no wait ever ran out.  With clear != 0 the word is reset after reading.
  */
 int mxq_watchdog_read(uint32_t* host_value, int clear);
+
+/*
+ * Self-test of the bounded-wait mechanism: enqueues one small kernel that
+ * waits on a barrier nothing will ever complete.  The wait gives up after
+ * limit_ns nanoseconds (1 <= limit_ns <= 2e9), the kernel sets bit 31 of the
+ * watchdog word and returns normally; the context stays usable.  Used by the
+ * tests to exercise the failure path without faulting the GPU.
+ */
+int mxq_watchdog_selftest(uint64_t limit_ns, mxq_stream_t stream);
 
 #ifdef __cplusplus
 }

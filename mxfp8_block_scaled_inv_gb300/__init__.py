@@ -20,8 +20,9 @@ __all__ = [
     "mxq_inv_rope_group_quant", "mxq_weight_scale_bytes", "mxq_prepare_weight_scales",
     "mxq_bmm_workspace_bytes", "mxq_bmm_a8w8", "mxq_linear_workspace_bytes", "mxq_linear",
     "mxq_linear_noalloc",
-    "mxq_dequant_bf16", "mxq_scales_f32_to_e8m0", "mxq_watchdog_read", "mxq_arch_supported",
-    "mxq_version", "wo_a",
+    "mxq_dequant_bf16", "mxq_scales_f32_to_e8m0", "mxq_watchdog_read", "mxq_watchdog_selftest",
+    "mxq_arch_supported",
+    "mxq_version", "mxq_wo_a_workspace_bytes", "mxq_wo_a", "wo_a",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -64,6 +65,10 @@ _SIGNATURES = {
     "mxq_scales_f32_to_e8m0": (ctypes.c_int, [_vp, _i64, _vp, _vp, _vp]),
     "mxq_watchdog_read": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "mxq_linear_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp]),
+    "mxq_watchdog_selftest": (ctypes.c_int, [ctypes.c_uint64, _vp]),
+    "mxq_wo_a_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32]),
+    "mxq_wo_a": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _i64, _i32, _i32, _i32,
+                                _i32, _vp, _vp, _sz, _vp]),
 }
 
 
@@ -182,11 +187,11 @@ def mxq_linear(x, w, w_sf, out=None, ws=None, stream=None):
     N = w.shape[-2]
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    if ws is None:
-        ws = torch.empty(max(mxq_linear_workspace_bytes(M, N, K), 16), dtype=torch.uint8,
-                         device=x.device)
-    st = lib().mxq_linear(_ptr(x), _ptr(w), _ptr(w_sf), _ptr(out), M, N, K, _ptr(ws), ws.numel(),
-                          _stream(stream))
+    need = mxq_linear_workspace_bytes(M, N, K)
+    if ws is None and need > 0:
+        ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+    st = lib().mxq_linear(_ptr(x), _ptr(w), _ptr(w_sf), _ptr(out), M, N, K, _ptr(ws),
+                          0 if ws is None else ws.numel(), _stream(stream))
     _check("mxq_linear", st)
     return out
 
@@ -229,10 +234,31 @@ def mxq_watchdog_read(clear=False):
     return v.value
 
 
-def wo_a(x, pos, cos, sin, w, w_sf, R=64, out=None, codes=None, scales=None, err_flag=None,
-         stream=None):
-    """The fused wo_a projection as two library calls on one stream:
-    inverse RoPE + group quantisation, then the block-scaled batched GEMM."""
-    q, sc = mxq_inv_rope_group_quant(x, pos, cos, sin, R, q=codes, sc=scales,
-                                     err_flag=err_flag, stream=stream)
-    return mxq_bmm_a8w8(q, sc, w, w_sf, out=out, stream=stream)
+def mxq_watchdog_selftest(limit_ns=1_000_000, stream=None):
+    _check("mxq_watchdog_selftest", lib().mxq_watchdog_selftest(limit_ns, _stream(stream)))
+
+
+def mxq_wo_a_workspace_bytes(T, G, D, N):
+    return lib().mxq_wo_a_workspace_bytes(T, G, D, N)
+
+
+def mxq_wo_a(x, pos, cos, sin, w, w_sf, R=64, out=None, ws=None, err_flag=None, stream=None):
+    """The wo_a projection in one library call: x bf16 [T, G, D] -> out bf16 [T, G, N]
+    (one fused launch for T <= 64; quantiser + GEMM through `ws` otherwise)."""
+    T, G, D = x.shape
+    N = w.shape[1]
+    if out is None:
+        out = torch.empty((T, G, N), dtype=torch.bfloat16, device=x.device)
+    need = mxq_wo_a_workspace_bytes(T, G, D, N)
+    if ws is None and need > 0:
+        ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+    cs_ld = cos.stride(0) if cos is not None else 0
+    max_pos = cos.shape[0] if cos is not None else 0
+    st = lib().mxq_wo_a(_ptr(x), _ptr(pos), _ptr(cos), _ptr(sin), cs_ld, max_pos, _ptr(w), _ptr(w_sf),
+                        _ptr(out), T, G, D, N, R, _ptr(err_flag), _ptr(ws),
+                        0 if ws is None else ws.numel(), _stream(stream))
+    _check("mxq_wo_a", st)
+    return out
+
+
+wo_a = mxq_wo_a

@@ -200,6 +200,7 @@ int mxq_bmm_a8w8(const uint8_t* a_e4m3, const uint8_t* a_e8m0, const uint8_t* w_
 
 size_t mxq_linear_workspace_bytes(int64_t M, int32_t N, int32_t K) {
   if (M < 0 || N < 1 || K < 1) return 0;
+  if (M <= mxq::kFusedMaxTokens) return 0;  // one fused launch, no scratch
   return round256((size_t)M * K) + round256((size_t)M * kgroups(K)) +
          round256(mxq_bmm_workspace_bytes(M, 1, N, K));
 }
@@ -215,6 +216,18 @@ int mxq_linear(const void* x_bf16, const uint8_t* w_e4m3, const uint8_t* w_sf_pr
     return fail(MXQ_ERR_NULL, "a NULL operand pointer");
   if (!aligned16(x_bf16) || !aligned16(w_e4m3) || !aligned16(w_sf_prepared) || !aligned16(out_bf16))
     return fail(MXQ_ERR_ALIGN, "operands must be 16-byte aligned");
+  if (K > 65536) return fail(MXQ_ERR_UNSUPPORTED, "K > 65536");
+  if (M <= mxq::kFusedMaxTokens) {
+    // Few rows: one launch that quantises x inside the GEMM.
+    int sms = 0;
+    if (int st = device_check(&sms)) return st;
+    const char* why = nullptr;
+    cudaError_t e = mxq::launch_wo_a_fused(x_bf16, nullptr, nullptr, nullptr, 0, 0, 0, w_e4m3,
+                                           w_sf_prepared, out_bf16, M, 1, N, K, nullptr, sms,
+                                           static_cast<cudaStream_t>(stream), &why);
+    if (e != cudaSuccess && why) return fail(MXQ_ERR_CUDA, "linear: %s", why);
+    return cuda_status(e, "linear (fused) launch");
+  }
   const size_t need = mxq_linear_workspace_bytes(M, N, K);
   if (!ws || ws_bytes < need)
     return fail(MXQ_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, ws_bytes);
@@ -227,6 +240,63 @@ int mxq_linear(const void* x_bf16, const uint8_t* w_e4m3, const uint8_t* w_sf_pr
     return st;
   return mxq_bmm_a8w8(codes, scales, w_e4m3, w_sf_prepared, out_bf16, M, 1, N, K, gemm_ws,
                       ws_bytes - (size_t)(gemm_ws - codes), stream);
+}
+
+size_t mxq_wo_a_workspace_bytes(int64_t T, int32_t G, int32_t D, int32_t N) {
+  (void)N;
+  if (T < 0 || G < 1 || D < 1) return 0;
+  if (T <= mxq::kFusedMaxTokens) return 0;
+  return round256((size_t)T * G * D) + round256((size_t)T * G * kgroups(D));
+}
+
+int mxq_wo_a(const void* x_bf16, const int64_t* pos, const void* cos_bf16, const void* sin_bf16,
+             int64_t cs_ld, int64_t max_pos, const uint8_t* w_e4m3, const uint8_t* w_sf_prepared,
+             void* out_bf16, int64_t T, int32_t G, int32_t D, int32_t N, int32_t R,
+             int32_t* err_flag, void* ws, size_t ws_bytes, mxq_stream_t stream) {
+  // Same argument rules as mxq_inv_rope_group_quant followed by mxq_bmm_a8w8.
+  if (T < 0 || G < 1 || D < 16 || R < 0 || N < 16)
+    return fail(MXQ_ERR_SHAPE, "need T >= 0, G >= 1, D >= 16, R >= 0, N >= 16");
+  if (D % 16 != 0 || N % 16 != 0) return fail(MXQ_ERR_SHAPE, "need D %% 16 == 0 and N %% 16 == 0");
+  if (D > 65536 || G > 65535) return fail(MXQ_ERR_UNSUPPORTED, "D > 65536 or G > 65535");
+  if (T == 0) return ok();
+  if (R > 0) {
+    if (R % 16 != 0 || R > 128 || R > D)
+      return fail(MXQ_ERR_UNSUPPORTED, "R must be a multiple of 16, <= 128 and <= D (R=%d)", R);
+    if (D % 128 != 0) return fail(MXQ_ERR_UNSUPPORTED, "R > 0 needs D %% 128 == 0 (D=%d)", D);
+    if (max_pos < 1 || cs_ld < R / 2)
+      return fail(MXQ_ERR_SHAPE, "need max_pos >= 1 and cs_ld >= R/2");
+    if (cs_ld % 8 != 0) return fail(MXQ_ERR_ALIGN, "cs_ld %% 8 != 0");
+    if (!pos || !cos_bf16 || !sin_bf16) return fail(MXQ_ERR_NULL, "pos/cos/sin is NULL with R > 0");
+    if (!aligned16(cos_bf16) || !aligned16(sin_bf16) || (reinterpret_cast<uintptr_t>(pos) & 7u))
+      return fail(MXQ_ERR_ALIGN, "cos/sin must be 16-byte aligned and pos 8-byte aligned");
+  }
+  if (!x_bf16 || !w_e4m3 || !w_sf_prepared || !out_bf16)
+    return fail(MXQ_ERR_NULL, "a NULL operand pointer");
+  if (!aligned16(x_bf16) || !aligned16(w_e4m3) || !aligned16(w_sf_prepared) || !aligned16(out_bf16))
+    return fail(MXQ_ERR_ALIGN, "operands must be 16-byte aligned");
+  if (err_flag && (reinterpret_cast<uintptr_t>(err_flag) & 3u))
+    return fail(MXQ_ERR_ALIGN, "err_flag must be 4-byte aligned");
+  if (T <= mxq::kFusedMaxTokens) {
+    int sms = 0;
+    if (int st = device_check(&sms)) return st;
+    const char* why = nullptr;
+    cudaError_t e = mxq::launch_wo_a_fused(x_bf16, pos, cos_bf16, sin_bf16, cs_ld, max_pos, R,
+                                           w_e4m3, w_sf_prepared, out_bf16, T, G, N, D, err_flag,
+                                           sms, static_cast<cudaStream_t>(stream), &why);
+    if (e != cudaSuccess && why) return fail(MXQ_ERR_CUDA, "wo_a: %s", why);
+    return cuda_status(e, "wo_a (fused) launch");
+  }
+  const size_t need = mxq_wo_a_workspace_bytes(T, G, D, N);
+  if (!ws || ws_bytes < need)
+    return fail(MXQ_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, ws_bytes);
+  if (!aligned16(ws)) return fail(MXQ_ERR_ALIGN, "workspace must be 16-byte aligned");
+  uint8_t* codes = static_cast<uint8_t*>(ws);
+  uint8_t* scales = codes + round256((size_t)T * G * D);
+  if (int st = mxq_inv_rope_group_quant(x_bf16, T, G, D, R, pos, cos_bf16, sin_bf16, cs_ld, max_pos,
+                                        codes, scales, err_flag, stream))
+    return st;
+  return mxq_bmm_a8w8(codes, scales, w_e4m3, w_sf_prepared, out_bf16, T, G, N, D, nullptr, 0,
+                      stream);
 }
 
 int mxq_dequant_bf16(const uint8_t* w_e4m3, const uint8_t* w_e8m0, void* out_bf16, int32_t B,
@@ -267,6 +337,15 @@ int mxq_watchdog_read(uint32_t* host_value, int clear) {
   int sms = 0;
   if (int st = device_check(&sms)) return st;
   return cuda_status(mxq::watchdog_read(host_value, clear != 0), "watchdog read");
+}
+
+int mxq_watchdog_selftest(uint64_t limit_ns, mxq_stream_t stream) {
+  if (limit_ns < 1 || limit_ns > 2000000000ull)
+    return fail(MXQ_ERR_SHAPE, "limit_ns must be in [1, 2e9]");
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  return cuda_status(mxq::launch_watchdog_selftest(limit_ns, static_cast<cudaStream_t>(stream)),
+                     "watchdog self-test launch");
 }
 
 }  // extern "C"

@@ -9,29 +9,46 @@
 //   out[t, g, n] = bf16( sum_k A[t,g,k] * W[g,n,k] ),
 //   A = E4M3(a) * 2^(sa-127), W = E4M3(w) * 2^(sw-127), one scale per 128 k.
 //
-// Design (one CTA = one 128 x BN output tile of one group g, optionally one
-// K-slice of it):
-//   warp 0      producer: TMA (128B-swizzled) loads of the A and W tiles for
-//               one 128-wide K group per pipeline stage, a bulk copy of the
-//               prepared weight-scale atom(s), and a gather of the
-//               activation scale bytes into the same 512-byte atom layout.
+// Work unit = one 128 x BN output tile of one group g (and, for the split-K
+// form, one K slice of it).  Warp roles (11 warps):
+//   warp 0      producer: per pipeline stage (one 128-wide K group) TMA loads
+//               of the A and W tiles (128-byte swizzle, zero fill outside the
+//               tensor: this is the unaligned-K tail), a bulk copy of the
+//               prepared weight-scale atom(s), and the activation-scale atom
+//               built from the compact scale buffer in shared memory.
 //   warp 1      TMEM owner and MMA issuer: per stage, tcgen05.cp of the scale
-//               atoms into TMEM, then four tcgen05.mma kind::mxf8f6f4
-//               block_scale (K = 32 each; the group's byte is replicated in
-//               all four bytes of its word, so every 32-block sees the
-//               group scale), then tcgen05.commit to free the stage.
-//   warps 2-5   epilogue: tcgen05.ld of the fp32 accumulator, RNE to BF16,
-//               stores.
-// The K tail is the TMA's zero fill past K.  Two orientations:
-//   normal  (many tokens): MMA M = 128 tokens, MMA N = BN weight rows.
-//   swapped (few tokens):  MMA M = 128 weight rows, MMA N = BN tokens, so the
-//               weight streams through the tensor cores with no padding of
-//               the token axis to 128.  The K range may be split over the
-//               CTAs of a thread-block cluster, whose fp32 partial tiles are
-//               summed in rank order through distributed shared memory
-//               (deterministic, no global workspace).
+//               atoms into TMEM, four tcgen05.mma kind::mxf8f6f4 block_scale
+//               (K = 32 each; every word of an atom holds its group's byte four
+//               times, so each 32-block sees the group scale), tcgen05.commit
+//               to free the stage; per tile a commit that hands the fp32
+//               accumulator to the epilogue.
+//   warp 2      activation-scale loader: copies the tile's scale bytes (one
+//               row per token, up to 64 groups at a time) from global memory
+//               into a double-buffered compact buffer ahead of the producer,
+//               so the producer never waits on a global load.
+//   warps 3-10  epilogue: two warps per TMEM lane quadrant, each draining half
+//               of the tile's columns into registers, then releasing the
+//               accumulator to the MMA warp before rounding to BF16 and
+//               storing, so the next tile's MMAs overlap the stores.
+// Two orientations:
+//   normal  (many tokens): MMA M = 128 tokens, MMA N = 256 weight rows; the
+//           CTAs are persistent and walk the tiles with the weight tile
+//           fastest, so concurrent CTAs share A and W tiles through L2.
+//   swapped (few tokens):  MMA M = 128 weight rows, MMA N = 16..128 tokens, so
+//           the weight streams at full tile width with no padding of the token
+//           axis to 128.  The K range may be split over the CTAs of a
+//           thread-block cluster, whose fp32 partial tiles are summed in rank
+//           order through distributed shared memory (deterministic, no global
+//           workspace).
+// Fused activation form (swapped orientation, T <= 64): the activation is
+// read as BF16 straight from the attention output by TMA, and the epilogue
+// warps, idle during the mainloop, quantise each stage's tokens (inverse
+// RoPE on the last group, group-128 E8M0 scale, E4M3 codes) directly into
+// the 128-byte-swizzled operand tile and the scale atom the MMA reads.  One
+// launch then does the whole wo_a (or MXFP8 linear) step, with no round trip
+// of the codes through HBM.
 // Every wait is bounded in wall time; on expiry the kernel sets a watchdog
-// bit, drains its own copies, frees TMEM and returns.
+// bit, stops issuing, drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -43,6 +60,7 @@
 #include "mxq.h"
 #include "mxq_internal.h"
 #include "mxq_ptx.cuh"
+#include "quant_common.cuh"
 
 namespace mxq {
 
@@ -51,35 +69,53 @@ __device__ uint32_t g_watchdog;
 namespace {
 
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
-constexpr uint32_t kWdProducer = 1, kWdMma = 2, kWdEpilogue = 4, kWdDrain = 8;
-constexpr int kThreads = 192;
+constexpr uint32_t kWdProducer = 1, kWdMma = 2, kWdEpilogue = 4, kWdDrain = 8, kWdLoader = 16;
+constexpr int kWarps = 11;
+constexpr int kThreads = kWarps * 32;
+constexpr int kEpiWarp0 = 3;
+constexpr int kSfChunk = 64;  // K groups held by one compact activation-scale buffer
 
 struct BmmArgs {
   const uint8_t* a_sf;  // [T][G][KG]
   const uint8_t* w_sf;  // prepared: [G][KG][NB][512]
   __nv_bfloat16* out;   // [T][G][N]
   int T, G, N, K, KG, NB;
-  int x_tiles, y_tiles;
+  int x_tiles, y_tiles;  // tiles along the MMA-A rows (128) and MMA-B rows (BN)
   int splits, kg_per_split;
+  int units;             // G * x_tiles * y_tiles * splits
+  int persistent;        // 1: each CTA walks units with stride gridDim.x
+  // Fused activation form only: positions, cos/sin cache, RoPE width.
+  const int64_t* pos;
+  const uint16_t* cos_tab;
+  const uint16_t* sin_tab;
+  int64_t cs_ld, max_pos;
+  int R;
+  int32_t* err_flag;
 };
 
-template <bool SWAP, int BN, int NSTAGE>
+template <bool SWAP, bool FUSED, int BN, int NSTAGE>
 struct Cfg {
   static constexpr int BM = 128;
   static constexpr int BK = 128;
   static constexpr int Y_ATOMS = (BN + 127) / 128;
-  static constexpr int ACT_ATOMS = SWAP ? Y_ATOMS : 1;
+  static constexpr int ACT_ROWS = SWAP ? BN : BM;
   static constexpr int X_TILE = BM * BK;
   static constexpr int Y_TILE = BN * BK;
   static constexpr int SFX_BYTES = kSfAtomBytes;
   static constexpr int SFY_BYTES = Y_ATOMS * kSfAtomBytes;
   static constexpr int W_SF_BYTES = (SWAP ? 1 : Y_ATOMS) * kSfAtomBytes;
+  static constexpr int CSF_BYTES = FUSED ? 0 : kSfChunk * 128;  // [group][128 rows]
+  static constexpr int STG_BYTES = FUSED ? BN * 256 : 0;         // BF16 staging [BN][128]
   static constexpr int OFF_X = 0;
   static constexpr int OFF_Y = OFF_X + NSTAGE * X_TILE;
   static constexpr int OFF_SFX = OFF_Y + NSTAGE * Y_TILE;
   static constexpr int OFF_SFY = OFF_SFX + NSTAGE * SFX_BYTES;
-  static constexpr int OFF_BAR = OFF_SFY + NSTAGE * SFY_BYTES;
-  static constexpr int N_BARS = 2 * NSTAGE + 1;
+  static constexpr int OFF_STG = OFF_SFY + NSTAGE * SFY_BYTES;
+  static constexpr int OFF_CSF = OFF_STG + NSTAGE * STG_BYTES;
+  static constexpr int OFF_BAR = OFF_CSF + 2 * CSF_BYTES;
+  // full[NSTAGE], empty[NSTAGE], landed[NSTAGE], acc_full, acc_empty,
+  // sf_full[2], sf_empty[2], mma_done
+  static constexpr int N_BARS = 3 * NSTAGE + 7;
   static constexpr int OFF_SLOT = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_SLOT + 16 + 1024;
   static constexpr int SF_COLS = 4 + 4 * Y_ATOMS;
@@ -89,6 +125,7 @@ struct Cfg {
                                    : TMEM_USED <= 128 ? 128
                                    : TMEM_USED <= 256 ? 256
                                                       : 512;
+  static constexpr int HALF = BN / 2;        // columns drained by one epilogue warp
   static constexpr int PART_PITCH = BN + 1;  // fp32 partial tile [128][BN+1] (aliases stages)
   // Instruction descriptor, kind::mxf8f6f4 with block scaling: E4M3 A and
   // B (format 0), both K-major, N >> 3 at bits 17-22, UE8M0 scale type at
@@ -97,8 +134,11 @@ struct Cfg {
       (1u << 23) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(128 * PART_PITCH * 4 <= OFF_BAR, "partial tile must fit in the stage buffers");
+  static_assert(128 * PART_PITCH * 4 <= OFF_SFX, "partial tile must fit in the operand buffers");
+  static_assert(!FUSED || (SWAP && BN <= 64), "fused activations: swapped form, <= 64 tokens");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+  static_assert(ACT_ROWS <= 128, "activation scale rows fit one loader pass");
+  static_assert(HALF % 8 == 0, "epilogue drains 8-column chunks");
 };
 
 __device__ __forceinline__ void watchdog(volatile int* abort_flag, uint32_t bit) {
@@ -106,43 +146,83 @@ __device__ __forceinline__ void watchdog(volatile int* abort_flag, uint32_t bit)
   atomicOr(&g_watchdog, bit);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
+  __nv_bfloat162 r = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
-template <bool SWAP, int BN, int NSTAGE>
+// Decoded work unit.  The weight tile index runs fastest.
+struct Unit {
+  int g, x0, y0, split, kg_begin, nk;
+};
+
+template <bool SWAP, int BN>
+__device__ __forceinline__ Unit decode_unit(const BmmArgs& p, int u) {
+  Unit w;
+  w.split = u % p.splits;
+  int r = u / p.splits;
+  int xt, yt;
+  if (!SWAP) {  // weights on Y
+    yt = r % p.y_tiles;
+    r /= p.y_tiles;
+    xt = r % p.x_tiles;
+    r /= p.x_tiles;
+  } else {  // weights on X
+    xt = r % p.x_tiles;
+    r /= p.x_tiles;
+    yt = r % p.y_tiles;
+    r /= p.y_tiles;
+  }
+  w.g = r;
+  w.x0 = xt * 128;
+  w.y0 = yt * BN;
+  w.kg_begin = w.split * p.kg_per_split;
+  w.nk = max(0, min(p.KG, w.kg_begin + p.kg_per_split) - w.kg_begin);
+  return w;
+}
+
+template <bool SWAP, bool FUSED, int BN, int NSTAGE>
 __global__ void __launch_bounds__(kThreads, 1)
     bmm_a8w8_kernel(const __grid_constant__ CUtensorMap tm_act,
                     const __grid_constant__ CUtensorMap tm_w, const BmmArgs p) {
-  using C = Cfg<SWAP, BN, NSTAGE>;
+  using C = Cfg<SWAP, FUSED, BN, NSTAGE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + NSTAGE;
-  uint64_t* acc_full = empty + NSTAGE;
+  uint64_t* landed = empty + NSTAGE;  // fused form: a stage's copies have landed
+  uint64_t* acc_full = landed + NSTAGE;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* sf_full = acc_empty + 1;
+  uint64_t* sf_empty = sf_full + 2;
+  uint64_t* mma_done = sf_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_SLOT);
+  uint8_t* csf = smem + C::OFF_CSF;
   __shared__ int abort_shared;
   volatile int* abort_flag = &abort_shared;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int split = blockIdx.x % p.splits;
-  const int tile = blockIdx.x / p.splits;
-  const int g = blockIdx.y;
-  const int x0 = (tile % p.x_tiles) * C::BM;  // first row of the MMA-A operand
-  const int y0 = (tile / p.x_tiles) * BN;     // first row of the MMA-B operand
-  const int kg_begin = split * p.kg_per_split;
-  const int kg_end = min(p.KG, kg_begin + p.kg_per_split);
-  const int nk = max(0, kg_end - kg_begin);
+  const int u_first = blockIdx.x;
+  const int u_step = p.persistent ? (int)gridDim.x : p.units;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
-      ptx::mbar_init(&full[s], 2);  // producer's expect_tx arrival + scale-gather arrival
+      // Unfused: the producer's weight arrival (with byte count) + its
+      // scale-atom arrival.  Fused: one arrival per quantising warp; the
+      // copies are tracked by `landed`.
+      ptx::mbar_init(&full[s], FUSED ? kWarps - kEpiWarp0 : 2);
       ptx::mbar_init(&empty[s], 1);
+      ptx::mbar_init(&landed[s], 1);
     }
     ptx::mbar_init(acc_full, 1);
+    ptx::mbar_init(acc_empty, kWarps - kEpiWarp0);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&sf_full[b], 32);
+      ptx::mbar_init(&sf_empty[b], 1);
+    }
+    ptx::mbar_init(mma_done, 1);
     abort_shared = 0;
     ptx::fence_barrier_init();
   }
@@ -160,169 +240,438 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // Activation scale rows handled by this lane: atom a, word j <-> row
-    // a*128 + 32*j + lane of the activation operand.
-    const int act_rows = SWAP ? BN : C::BM;
-    const int act_row0 = SWAP ? y0 : x0;
-    uint32_t words[4 * C::ACT_ATOMS];
-    auto gather = [&](int kg) {
-#pragma unroll
-      for (int a = 0; a < C::ACT_ATOMS; ++a)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = a * 128 + 32 * j + lane;
-          const int t = act_row0 + r;
-          uint32_t b = 127u;
-          if (r < act_rows && t < p.T) b = __ldg(p.a_sf + ((size_t)t * p.G + g) * p.KG + kg);
-          words[a * 4 + j] = b * 0x01010101u;
-        }
+    if constexpr (FUSED) {
+    // ----------------------------------------------- producer (fused form)
+    // `landed[s]` collects every copy of stage s: the weight tile and scale
+    // atom (issued early, before waiting for the preceding kernel) and the
+    // BF16 activation tile; its single arrival comes after all are issued.
+    int it = 0, issued = 0;
+    bool stop = false;
+    auto issue_weights = [&](const Unit& w, int s, int kg) {
+      ptx::mbar_expect_tx(&landed[s], C::X_TILE + C::W_SF_BYTES);
+      ptx::tma_load_3d(smem + C::OFF_X + s * C::X_TILE, &tm_w, &landed[s], kg * 128, w.x0, w.g);
+      ptx::bulk_load(smem + C::OFF_SFX + s * C::SFX_BYTES,
+                     p.w_sf + (((size_t)w.g * p.KG + kg) * p.NB + w.x0 / 128) * kSfAtomBytes,
+                     C::W_SF_BYTES, &landed[s]);
     };
-    int issued = 0;
-    if (nk > 0) gather(kg_begin);
-    for (int it = 0; it < nk; ++it) {
-      const int s = it % NSTAGE;
-      const uint32_t ph = (uint32_t)(it / NSTAGE) & 1u;
-      if (*abort_flag) break;
-      if (!ptx::mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs)) {
-        watchdog(abort_flag, kWdProducer);
-        break;
-      }
-      const int kg = kg_begin + it;
-      uint8_t* xs = smem + C::OFF_X + s * C::X_TILE;
-      uint8_t* ys = smem + C::OFF_Y + s * C::Y_TILE;
-      uint8_t* sfx = smem + C::OFF_SFX + s * C::SFX_BYTES;
-      uint8_t* sfy = smem + C::OFF_SFY + s * C::SFY_BYTES;
-      if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(&full[s], C::X_TILE + C::Y_TILE + C::W_SF_BYTES);
-        if (!SWAP) {
-          ptx::tma_load_3d(xs, &tm_act, &full[s], kg * 128, g, x0);
-          ptx::tma_load_3d(ys, &tm_w, &full[s], kg * 128, y0, g);
-          ptx::bulk_load(sfy, p.w_sf + (((size_t)g * p.KG + kg) * p.NB + y0 / 128) * kSfAtomBytes,
-                         C::W_SF_BYTES, &full[s]);
-        } else {
-          ptx::tma_load_3d(xs, &tm_w, &full[s], kg * 128, x0, g);
-          ptx::tma_load_3d(ys, &tm_act, &full[s], kg * 128, g, y0);
-          ptx::bulk_load(sfx, p.w_sf + (((size_t)g * p.KG + kg) * p.NB + x0 / 128) * kSfAtomBytes,
-                         C::W_SF_BYTES, &full[s]);
-        }
-      }
-      uint8_t* act_sf = SWAP ? sfy : sfx;
-#pragma unroll
-      for (int a = 0; a < C::ACT_ATOMS; ++a)
-        *reinterpret_cast<uint4*>(act_sf + a * kSfAtomBytes + lane * 16) =
-            make_uint4(words[4 * a], words[4 * a + 1], words[4 * a + 2], words[4 * a + 3]);
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&full[s]);
-      ++issued;
-      if (it + 1 < nk) gather(kg + 1);
+    if (u_first < p.units) {
+      const Unit w = decode_unit<SWAP, BN>(p, u_first);
+      issued = min(w.nk, NSTAGE);
+      if (lane == 0)
+        for (int kk = 0; kk < issued; ++kk) issue_weights(w, kk, w.kg_begin + kk);
     }
-    // Drain: every issued stage's copies must have landed before exit.
-    for (int it = max(0, issued - NSTAGE); it < issued; ++it) {
-      if (!ptx::mbar_wait(&full[it % NSTAGE], (uint32_t)(it / NSTAGE) & 1u, kWaitLimitNs)) {
+    ptx::griddep_wait();
+    for (int u = u_first; u < p.units && !stop; u += u_step) {
+      const Unit w = decode_unit<SWAP, BN>(p, u);
+      for (int kk = 0; kk < w.nk; ++kk) {
+        const int s = it % NSTAGE;
+        const uint32_t ph = (uint32_t)(it / NSTAGE) & 1u;
+        const int kg = w.kg_begin + kk;
+        if (it >= issued) {
+          if (*abort_flag || !ptx::mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs)) {
+            if (!*abort_flag) watchdog(abort_flag, kWdProducer);
+            stop = true;
+            break;
+          }
+          if (lane == 0) issue_weights(w, s, kg);
+          ++issued;
+        }
+        if (lane == 0) {
+          ptx::mbar_expect_tx(&landed[s], C::STG_BYTES);
+          ptx::tma_load_3d(smem + C::OFF_STG + s * C::STG_BYTES, &tm_act, &landed[s], kg * 128, w.g,
+                           w.y0);
+          ptx::mbar_arrive(&landed[s]);
+        }
+        __syncwarp();
+        ++it;
+      }
+    }
+    if (lane == 0)
+      for (int j = it; j < issued; ++j) ptx::mbar_arrive(&landed[j % NSTAGE]);
+    __syncwarp();
+    for (int j = max(0, issued - NSTAGE); j < issued; ++j) {
+      if (!ptx::mbar_wait(&landed[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1u, kWaitLimitNs)) {
         watchdog(abort_flag, kWdDrain);
         break;
       }
     }
+    } else {
+    // ------------------------------------------------------------ producer
+    // Stage bookkeeping (counters continue across units): stages < `it` are
+    // complete on the producer side; stages < `issued` have their weight
+    // copies in flight.  A stage's full barrier takes two arrivals (weights,
+    // with their byte count; then the activation-scale atom) plus the bytes
+    // of the activation tile, announced when that copy is issued.
+    int it = 0, issued = 0, ci = 0;
+    bool stop = false;
+    auto issue_weights = [&](const Unit& w, int s, int kg) {
+      uint8_t* wt = smem + (SWAP ? C::OFF_X + s * C::X_TILE : C::OFF_Y + s * C::Y_TILE);
+      uint8_t* wsf = smem + (SWAP ? C::OFF_SFX + s * C::SFX_BYTES : C::OFF_SFY + s * C::SFY_BYTES);
+      const int wrow0 = SWAP ? w.x0 : w.y0;
+      ptx::mbar_arrive_expect_tx(&full[s], (SWAP ? C::X_TILE : C::Y_TILE) + C::W_SF_BYTES);
+      ptx::tma_load_3d(wt, &tm_w, &full[s], kg * 128, wrow0, w.g);
+      ptx::bulk_load(wsf, p.w_sf + (((size_t)w.g * p.KG + kg) * p.NB + wrow0 / 128) * kSfAtomBytes,
+                     C::W_SF_BYTES, &full[s]);
+    };
+    // Weight tiles and scales do not depend on the preceding kernel: the
+    // first unit's first stages of weights are issued before waiting for it
+    // (programmatic dependent launch), so the weight stream starts while the
+    // quantiser is still finishing.
+    if (u_first < p.units) {
+      const Unit w = decode_unit<SWAP, BN>(p, u_first);
+      issued = min(w.nk, NSTAGE);
+      if (lane == 0)
+        for (int kk = 0; kk < issued; ++kk) issue_weights(w, kk, w.kg_begin + kk);
+    }
+    ptx::griddep_wait();
+    for (int u = u_first; u < p.units && !stop; u += u_step) {
+      const Unit w = decode_unit<SWAP, BN>(p, u);
+      for (int kk = 0; kk < w.nk; ++kk) {
+        const int b = ci & 1;
+        const int s = it % NSTAGE;
+        const uint32_t ph = (uint32_t)(it / NSTAGE) & 1u;
+        const int kg = w.kg_begin + kk;
+        if (it >= issued) {
+          if (*abort_flag || !ptx::mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs)) {
+            if (!*abort_flag) watchdog(abort_flag, kWdProducer);
+            stop = true;
+            break;
+          }
+          if (lane == 0) issue_weights(w, s, kg);
+          ++issued;
+        }
+        if ((kk % kSfChunk) == 0 &&
+            !ptx::mbar_wait(&sf_full[b], (uint32_t)(ci >> 1) & 1u, kWaitLimitNs)) {
+          watchdog(abort_flag, kWdProducer);
+          stop = true;
+          break;
+        }
+        if (lane == 0) {
+          uint8_t* at = smem + (SWAP ? C::OFF_Y + s * C::Y_TILE : C::OFF_X + s * C::X_TILE);
+          ptx::mbar_expect_tx(&full[s], SWAP ? C::Y_TILE : C::X_TILE);
+          ptx::tma_load_3d(at, &tm_act, &full[s], kg * 128, w.g, SWAP ? w.y0 : w.x0);
+        }
+        // Activation-scale atom: lane i writes the 16-byte line of rows
+        // i, i+32, i+64, i+96 (one word each, the byte replicated four times).
+        const uint8_t* col = csf + b * C::CSF_BYTES + (kk % kSfChunk) * 128;
+        uint4 line;
+        line.x = (uint32_t)col[lane] * 0x01010101u;
+        line.y = (uint32_t)col[lane + 32] * 0x01010101u;
+        line.z = (uint32_t)col[lane + 64] * 0x01010101u;
+        line.w = (uint32_t)col[lane + 96] * 0x01010101u;
+        uint8_t* asf = smem + (SWAP ? C::OFF_SFY + s * C::SFY_BYTES : C::OFF_SFX + s * C::SFX_BYTES);
+        *reinterpret_cast<uint4*>(asf + lane * 16) = line;
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&full[s]);
+        ++it;
+        if ((kk % kSfChunk) == kSfChunk - 1 || kk == w.nk - 1) {
+          if (lane == 0) ptx::mbar_arrive(&sf_empty[b]);
+          ++ci;
+        }
+      }
+    }
+    // After an abort, stages with weights in flight but no second arrival get
+    // it now, so that their phase completes once the copies have landed.
+    if (lane == 0)
+      for (int j = it; j < issued; ++j) ptx::mbar_arrive(&full[j % NSTAGE]);
+    __syncwarp();
+    // Drain: every issued copy must have landed before exit.
+    for (int j = max(0, issued - NSTAGE); j < issued; ++j) {
+      if (!ptx::mbar_wait(&full[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1u, kWaitLimitNs)) {
+        watchdog(abort_flag, kWdDrain);
+        break;
+      }
+    }
+    }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
-    for (int it = 0; it < nk; ++it) {
-      const int s = it % NSTAGE;
-      const uint32_t ph = (uint32_t)(it / NSTAGE) & 1u;
-      if (*abort_flag) break;
-      if (!ptx::mbar_wait(&full[s], ph, kWaitLimitNs)) {
-        watchdog(abort_flag, kWdMma);
+    int it = 0, ti = 0;
+    bool stop = false;
+    for (int u = u_first; u < p.units && !stop; u += u_step) {
+      const Unit w = decode_unit<SWAP, BN>(p, u);
+      if (*abort_flag || !ptx::mbar_wait(acc_empty, (uint32_t)(ti & 1) ^ 1u, kWaitLimitNs)) {
+        if (!*abort_flag) watchdog(abort_flag, kWdMma);
         break;
       }
       ptx::tc_fence_after();
-      if (lane == 0) {
-        const uint32_t sfx_col = tmem + BN + s * C::SF_COLS;
-        const uint32_t sfy_col = sfx_col + 4;
-        const uint32_t xs = ptx::smem_u32(smem + C::OFF_X + s * C::X_TILE);
-        const uint32_t ys = ptx::smem_u32(smem + C::OFF_Y + s * C::Y_TILE);
-        const uint32_t sfx = ptx::smem_u32(smem + C::OFF_SFX + s * C::SFX_BYTES);
-        const uint32_t sfy = ptx::smem_u32(smem + C::OFF_SFY + s * C::SFY_BYTES);
-        ptx::tmem_cp_32x128b_x4(sfx_col, ptx::smem_desc(sfx, 128, 128, ptx::kSwizzleNone));
+      for (int kk = 0; kk < w.nk; ++kk) {
+        const int s = it % NSTAGE;
+        const uint32_t ph = (uint32_t)(it / NSTAGE) & 1u;
+        if (*abort_flag || !ptx::mbar_wait(&full[s], ph, kWaitLimitNs)) {
+          if (!*abort_flag) watchdog(abort_flag, kWdMma);
+          stop = true;
+          break;
+        }
+        ptx::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sfx_col = tmem + BN + s * C::SF_COLS;
+          const uint32_t sfy_col = sfx_col + 4;
+          const uint32_t xs = ptx::smem_u32(smem + C::OFF_X + s * C::X_TILE);
+          const uint32_t ys = ptx::smem_u32(smem + C::OFF_Y + s * C::Y_TILE);
+          const uint32_t sfx = ptx::smem_u32(smem + C::OFF_SFX + s * C::SFX_BYTES);
+          const uint32_t sfy = ptx::smem_u32(smem + C::OFF_SFY + s * C::SFY_BYTES);
+          ptx::tmem_cp_32x128b_x4(sfx_col, ptx::smem_desc(sfx, 128, 128, ptx::kSwizzleNone));
 #pragma unroll
-        for (int a = 0; a < C::Y_ATOMS; ++a)
-          ptx::tmem_cp_32x128b_x4(sfy_col + 4 * a, ptx::smem_desc(sfy + a * kSfAtomBytes, 128, 128,
-                                                                  ptx::kSwizzleNone));
-        const uint64_t adesc = ptx::smem_desc(xs, 16, 1024, ptx::kSwizzle128B);
-        const uint64_t bdesc = ptx::smem_desc(ys, 16, 1024, ptx::kSwizzle128B);
+          for (int a = 0; a < C::Y_ATOMS; ++a)
+            ptx::tmem_cp_32x128b_x4(
+                sfy_col + 4 * a,
+                ptx::smem_desc(sfy + a * kSfAtomBytes, 128, 128, ptx::kSwizzleNone));
+          const uint64_t adesc = ptx::smem_desc(xs, 16, 1024, ptx::kSwizzle128B);
+          const uint64_t bdesc = ptx::smem_desc(ys, 16, 1024, ptx::kSwizzle128B);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)  // 4 x (K = 32 bytes) inside the 128-byte swizzle row
-          ptx::mma_mxf8(tmem, adesc + 2 * k, bdesc + 2 * k, C::IDESC, sfx_col, sfy_col,
-                        (it > 0 || k > 0) ? 1u : 0u);
-        ptx::tc_commit(&empty[s]);
+          for (int k = 0; k < 4; ++k)  // 4 x (K = 32 bytes) inside the 128-byte swizzle row
+            ptx::mma_mxf8(tmem, adesc + 2 * k, bdesc + 2 * k, C::IDESC, sfx_col, sfy_col,
+                          (kk > 0 || k > 0) ? 1u : 0u);
+          ptx::tc_commit(&empty[s]);
+        }
+        __syncwarp();
+        ++it;
       }
+      if (stop) break;
+      if (lane == 0) ptx::tc_commit(acc_full);
       __syncwarp();
+      ++ti;
     }
-    if (lane == 0) ptx::tc_commit(acc_full);  // also after an abort: tracks what was issued
+    // Every MMA and scale copy this warp issued must finish before TMEM is freed.
+    if (lane == 0) ptx::tc_commit(mma_done);
     __syncwarp();
+    if (!ptx::mbar_wait(mma_done, 0, kWaitLimitNs)) watchdog(abort_flag, kWdDrain);
+  } else if (warp == 2) {
+    // ------------------------------------------------- activation scales
+    // (The fused form quantises in the epilogue warps and has no loader.)
+    if constexpr (!FUSED) {
+    int ci = 0;
+    bool stop = false;
+    for (int u = u_first; u < p.units && !stop; u += u_step) {
+      const Unit w = decode_unit<SWAP, BN>(p, u);
+      const int row0 = SWAP ? w.y0 : w.x0;
+      if (u == u_first) ptx::griddep_wait();  // the scales come from the preceding kernel
+      for (int c0 = 0; c0 < w.nk; c0 += kSfChunk) {
+        const int b = ci & 1;
+        if (*abort_flag ||
+            !ptx::mbar_wait(&sf_empty[b], ((uint32_t)(ci >> 1) & 1u) ^ 1u, kWaitLimitNs)) {
+          if (!*abort_flag) watchdog(abort_flag, kWdLoader);
+          stop = true;
+          break;
+        }
+        const int ng = min(kSfChunk, w.nk - c0);
+        const int kg0 = w.kg_begin + c0;
+        uint8_t* dst = csf + b * C::CSF_BYTES;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = 32 * j + lane;
+          const int t = row0 + r;
+          const bool valid = r < C::ACT_ROWS && t < p.T;
+          const uint8_t* src = p.a_sf + ((size_t)(valid ? t : 0) * p.G + w.g) * p.KG + kg0;
+          if (valid && ((p.KG | kg0 | ng) & 15) == 0) {
+            // 16-byte vectors: the row start and the chunk are 16-byte aligned.
+            uint4 v[kSfChunk / 16];
+#pragma unroll
+            for (int q = 0; q < kSfChunk / 16; ++q)
+              if (q * 16 < ng) v[q] = __ldg(reinterpret_cast<const uint4*>(src) + q);
+#pragma unroll
+            for (int q = 0; q < kSfChunk / 16; ++q) {
+              if (q * 16 >= ng) break;
+              const uint32_t wv[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                dst[(q * 16 + e) * 128 + r] = (uint8_t)(wv[e >> 2] >> (8 * (e & 3)));
+            }
+          } else if (valid) {
+            for (int q = 0; q < ng; ++q) dst[q * 128 + r] = __ldg(src + q);
+          } else {
+            for (int q = 0; q < ng; ++q) dst[q * 128 + r] = 127;
+          }
+        }
+        ptx::mbar_arrive(&sf_full[b]);  // every lane: its own stores are released
+        ++ci;
+      }
+    }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
-    const int r = q * 32 + lane;
-    const bool waited = ptx::mbar_wait(acc_full, 0, kWaitLimitNs);
-    if (!waited) watchdog(abort_flag, kWdEpilogue);
-    ptx::tc_fence_after();
-    const bool ok = __all_sync(0xffffffffu, waited) && !*abort_flag;
-    if (ok) {
-      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-      float* part = reinterpret_cast<float*>(smem);  // stage buffers are idle now
-#pragma unroll 1
-      for (int c = 0; c < BN / 16; ++c) {
-        uint32_t v[16];
-        ptx::tmem_ld_32x32b_x16(trow + c * 16, v);
-        ptx::tmem_ld_wait();
-        if (nk == 0) {
+    const int q = warp & 3;                       // TMEM lane quadrant this warp may access
+    const int h = (warp - kEpiWarp0) >> 2;        // which half of the columns
+    const int r = q * 32 + lane;                  // accumulator row (TMEM lane)
+    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + h * C::HALF;
+    float* part = reinterpret_cast<float*>(smem);  // split-K partial tile (stage buffers idle)
+    int ti = 0;
+    int itq = 0;  // stage counter of the fused activation quantisation
+    if constexpr (FUSED) {
+      // Scale-atom rows past the token tile (BN < 128) never change: 127.
+      const int te = threadIdx.x - kEpiWarp0 * 32;
+      for (int i = te; i < NSTAGE * (128 - BN); i += (kWarps - kEpiWarp0) * 32) {
+        const int s = i / (128 - BN);
+        const int rr = BN + i % (128 - BN);
+        *reinterpret_cast<uint32_t*>(smem + C::OFF_SFY + s * C::SFY_BYTES + (rr & 31) * 16 +
+                                     ((rr >> 5) & 3) * 4) = 0x7F7F7F7Fu;
+      }
+      ptx::griddep_wait();  // positions (and x, via TMA) come from preceding kernels
+    }
+    for (int u = u_first; u < p.units; u += u_step) {
+      const Unit w = decode_unit<SWAP, BN>(p, u);
+      if constexpr (FUSED) {
+        // ---------------------------------------- fused activation quantisation
+        // Half-warp per token: token slot = 16*pass + 2*e + half, lane `sub`
+        // holds elements [8*sub, 8*sub+8) of the stage's 128-wide group.
+        constexpr int PASSES = BN / 16;
+        const int e = warp - kEpiWarp0;
+        const int sub = lane & 15;
+        const int hw = lane >> 4;
+        const bool has_rope = p.R > 0 && w.kg_begin + w.nk == p.KG;
+        const int first = 16 - (p.R >> 3);
+        const int dist = p.R >> 4;
+        const bool rope_lane = p.R > 0 && sub >= first;
+        const bool lower = sub < first + dist;
+        const int partner = rope_lane ? (lower ? sub + dist : sub - dist) : sub;
+        bool bad[PASSES];
+        uint4 cw[PASSES], sw[PASSES];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = 0u;  // empty K slice contributes zero
-        }
-        if (!SWAP) {
-          const int t = x0 + r;
-          const int n = y0 + c * 16;
-          if (t < p.T && n < p.N) {
-            uint4 lo, hi;
-            lo.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
-            lo.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
-            lo.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
-            lo.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
-            hi.x = pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9]));
-            hi.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
-            hi.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
-            hi.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
-            uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)t * p.G + g) * p.N + n);
-            dst[0] = lo;
-            dst[1] = hi;
+        for (int ps = 0; ps < PASSES; ++ps) {
+          const int t = w.y0 + 16 * ps + 2 * e + hw;
+          int64_t pp = 0;
+          bad[ps] = false;
+          cw[ps] = make_uint4(0, 0, 0, 0);
+          sw[ps] = make_uint4(0, 0, 0, 0);
+          if (p.R > 0 && t < p.T) {
+            pp = __ldg(p.pos + t);
+            bad[ps] = pp < 0 || pp >= p.max_pos;
+            if (has_rope && rope_lane && !bad[ps]) {
+              const int i0 = (sub - first - (lower ? 0 : dist)) * 8;
+              cw[ps] = __ldg(reinterpret_cast<const uint4*>(p.cos_tab + pp * p.cs_ld + i0));
+              sw[ps] = __ldg(reinterpret_cast<const uint4*>(p.sin_tab + pp * p.cs_ld + i0));
+            }
+            if (bad[ps] && sub == 0 && w.x0 == 0 && w.split == 0 && p.err_flag != nullptr)
+              atomicOr(p.err_flag, MXQ_DEVERR_POSITION);
           }
-        } else if (p.splits == 1) {
-          const int n = x0 + r;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int t = y0 + c * 16 + j;
-            if (t < p.T && n < p.N)
-              p.out[((size_t)t * p.G + g) * p.N + n] = __float2bfloat16_rn(__uint_as_float(v[j]));
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) part[r * C::PART_PITCH + c * 16 + j] = __uint_as_float(v[j]);
         }
+        bool qstop = false;
+        for (int kk = 0; kk < w.nk; ++kk) {
+          const int s = itq % NSTAGE;
+          const uint32_t ph = (uint32_t)(itq / NSTAGE) & 1u;
+          const bool ok_wait = !*abort_flag && ptx::mbar_wait(&landed[s], ph, kWaitLimitNs);
+          if (!__all_sync(0xffffffffu, ok_wait)) {
+            if (!*abort_flag) watchdog(abort_flag, kWdEpilogue);
+            qstop = true;
+            break;
+          }
+          const bool rope = has_rope && w.kg_begin + kk == p.KG - 1;
+          const uint8_t* stg = smem + C::OFF_STG + s * C::STG_BYTES;
+          uint8_t* codes = smem + C::OFF_Y + s * C::Y_TILE;
+          uint8_t* atom = smem + C::OFF_SFY + s * C::SFY_BYTES;
+#pragma unroll
+          for (int ps = 0; ps < PASSES; ++ps) {
+            const int slot = 16 * ps + 2 * e + hw;
+            const bool valid = w.y0 + slot < p.T;
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + slot * 256 + sub * 16);
+            float y[8];
+            unpack8(v, y);
+            if (rope) {
+              const int src = (hw << 4) | partner;
+              uint4 pv;
+              pv.x = __shfl_sync(0xffffffffu, v.x, src);
+              pv.y = __shfl_sync(0xffffffffu, v.y, src);
+              pv.z = __shfl_sync(0xffffffffu, v.z, src);
+              pv.w = __shfl_sync(0xffffffffu, v.w, src);
+              if (rope_lane && valid && !bad[ps]) {
+                float xp[8];
+                unpack8(pv, xp);
+                inv_rope8(y, xp, cw[ps], sw[ps], lower);
+              }
+            }
+            const float amax = half_warp_amax(y);
+            uint32_t sbyte;
+            uint2 q8 = encode8(y, amax, &sbyte);
+            if (!valid) {  // padding token of the tile
+              q8 = make_uint2(0, 0);
+              sbyte = 127;
+            }
+            if (bad[ps]) {  // a token with an invalid position is zeroed
+              q8 = make_uint2(0, 0);
+              sbyte = 0;
+            }
+            // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8).
+            const int c16 = sub >> 1;
+            *reinterpret_cast<uint2*>(codes + slot * 128 + ((c16 ^ (slot & 7)) << 4) + ((sub & 1) << 3)) =
+                q8;
+            if (sub == 0)
+              *reinterpret_cast<uint32_t*>(atom + (slot >> 7) * kSfAtomBytes + (slot & 31) * 16 +
+                                           ((slot >> 5) & 3) * 4) = sbyte * 0x01010101u;
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&full[s]);
+          ++itq;
+        }
+        if (qstop) break;
+      }
+      const bool waited = !*abort_flag && ptx::mbar_wait(acc_full, (uint32_t)(ti & 1), kWaitLimitNs);
+      if (!__all_sync(0xffffffffu, waited)) {
+        if (!*abort_flag) watchdog(abort_flag, kWdEpilogue);
+        break;
+      }
+      ptx::tc_fence_after();
+      uint32_t v[C::HALF];
+      if constexpr (C::HALF % 32 == 0) {
+#pragma unroll
+        for (int c = 0; c < C::HALF / 32; ++c) ptx::tmem_ld_32x32b_x32(trow + c * 32, v + c * 32);
+      } else {
+#pragma unroll
+        for (int c = 0; c < C::HALF / 8; ++c) ptx::tmem_ld_32x32b_x8(trow + c * 8, v + c * 8);
+      }
+      ptx::tmem_ld_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(acc_empty);  // the accumulator may be overwritten now
+      ++ti;
+      if (w.nk == 0) {
+#pragma unroll
+        for (int j = 0; j < C::HALF; ++j) v[j] = 0u;  // an empty K slice contributes zero
+      }
+      const int c0 = h * C::HALF;
+      if (!SWAP) {
+        const int t = w.x0 + r;
+        if (t < p.T) {
+          __nv_bfloat16* orow = p.out + ((size_t)t * p.G + w.g) * p.N + w.y0 + c0;
+#pragma unroll
+          for (int c = 0; c < C::HALF / 8; ++c) {
+            if (w.y0 + c0 + c * 8 < p.N) {
+              uint4 o;
+              o.x = pack_bf16x2(v[c * 8 + 0], v[c * 8 + 1]);
+              o.y = pack_bf16x2(v[c * 8 + 2], v[c * 8 + 3]);
+              o.z = pack_bf16x2(v[c * 8 + 4], v[c * 8 + 5]);
+              o.w = pack_bf16x2(v[c * 8 + 6], v[c * 8 + 7]);
+              *reinterpret_cast<uint4*>(orow + c * 8) = o;
+            }
+          }
+        }
+      } else if (p.splits == 1) {
+        const int n = w.x0 + r;
+#pragma unroll
+        for (int j = 0; j < C::HALF; ++j) {
+          const int t = w.y0 + c0 + j;
+          if (t < p.T && n < p.N)
+            p.out[((size_t)t * p.G + w.g) * p.N + n] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < C::HALF; ++j) part[r * C::PART_PITCH + c0 + j] = __uint_as_float(v[j]);
       }
     }
-    ptx::tc_fence_before();
   }
 
   __syncthreads();
   if (SWAP && p.splits > 1) {
-    // Deterministic split-K reduction over the cluster: CTA `split` sums
-    // rows [split*rows, (split+1)*rows) of the tile over ranks 0..splits-1.
+    // Deterministic split-K reduction over the cluster (one unit per CTA):
+    // CTA `split` sums rows [split*rows, (split+1)*rows) of the tile over the
+    // ranks 0..splits-1 in order.
+    const Unit w = decode_unit<SWAP, BN>(p, u_first);
     ptx::cluster_sync();
     const int rows = (C::BM + p.splits - 1) / p.splits;
-    const int r_begin = split * rows;
+    const int r_begin = w.split * rows;
     const int r_end = min(C::BM, r_begin + rows);
-    const int tv = min(BN, p.T - y0);
+    const int tv = min(BN, p.T - w.y0);
     const int nrows = r_end - r_begin;
     if (!*abort_flag && nrows > 0 && tv > 0) {
       const uint32_t part0 = ptx::smem_u32(smem);
@@ -333,8 +682,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         float acc = 0.0f;
         for (int rk = 0; rk < p.splits; ++rk)
           acc += ptx::ld_shared_cluster_f32(ptx::map_shared_rank(part0 + off, (uint32_t)rk));
-        const int n = x0 + rr;
-        if (n < p.N) p.out[((size_t)(y0 + tl) * p.G + g) * p.N + n] = __float2bfloat16_rn(acc);
+        const int n = w.x0 + rr;
+        if (n < p.N)
+          p.out[((size_t)(w.y0 + tl) * p.G + w.g) * p.N + n] = __float2bfloat16_rn(acc);
       }
     }
     ptx::cluster_sync();  // keep every partial tile alive until all readers are done
@@ -343,6 +693,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::TMEM_COLS);
   }
+}
+
+// A kernel that waits on an mbarrier nobody arrives at: the bounded wait must
+// give up after `limit_ns` and record the expiry in the watchdog word.
+__global__ void watchdog_selftest_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !ptx::mbar_wait(&bar, 0, limit_ns)) atomicOr(&g_watchdog, 1u << 31);
+  __syncthreads();
 }
 
 // --------------------------------------------------------------- host side
@@ -360,9 +723,10 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// 3-D uint8 tensor map, inner dimension K with 128-byte rows swizzled, zero
-// fill outside the tensor.
-bool encode_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+// 3-D tensor map with zero fill outside the tensor: uint8 codes with
+// 128-byte rows swizzled (MMA operands), or BF16 rows unswizzled (the fused
+// form's activation staging).
+bool encode_3d(CUtensorMap* m, const void* base, bool bf16, uint64_t d0, uint64_t d1, uint64_t d2,
                uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2) {
   auto enc = get_encode();
   if (!enc) return false;
@@ -370,26 +734,28 @@ bool encode_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint6
   cuuint64_t strides[2] = {stride1, stride2};
   cuuint32_t box[3] = {b0, b1, b2};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
-                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   bf16 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <bool SWAP, int BN, int NSTAGE>
-cudaError_t launch_cfg(const uint8_t* a, const uint8_t* w, BmmArgs args, cudaStream_t s,
-                       const char** why) {
-  using C = Cfg<SWAP, BN, NSTAGE>;
+template <bool SWAP, bool FUSED, int BN, int NSTAGE>
+cudaError_t launch_cfg(const void* a, const uint8_t* w, BmmArgs args, int num_sms,
+                       cudaStream_t s, const char** why) {
+  using C = Cfg<SWAP, FUSED, BN, NSTAGE>;
   const uint64_t K = args.K, G = args.G, T = args.T, N = args.N;
   CUtensorMap tm_act, tm_w;
   const uint32_t act_box = SWAP ? BN : C::BM;
   const uint32_t w_box = SWAP ? C::BM : BN;
-  if (!encode_3d(&tm_act, a, K, G, T, K, G * K, 128, 1, act_box) ||
-      !encode_3d(&tm_w, w, K, N, G, K, N * K, 128, w_box, 1)) {
+  const uint64_t esz = FUSED ? 2 : 1;  // fused form: x is BF16
+  if (!encode_3d(&tm_act, a, FUSED, K, G, T, K * esz, G * K * esz, 128, 1, act_box) ||
+      !encode_3d(&tm_w, w, false, K, N, G, K, N * K, 128, w_box, 1)) {
     *why = "cuTensorMapEncodeTiled failed (driver entry point missing or arguments rejected)";
     return cudaErrorInvalidValue;
   }
-  auto kern = bmm_a8w8_kernel<SWAP, BN, NSTAGE>;
+  auto kern = bmm_a8w8_kernel<SWAP, FUSED, BN, NSTAGE>;
   // The shared-memory opt-in is set once per device (a host-side call that
   // must not run inside stream capture, so the first call on a device should
   // happen before any capture).
@@ -403,20 +769,28 @@ cudaError_t launch_cfg(const uint8_t* a, const uint8_t* w, BmmArgs args, cudaStr
     if (e != cudaSuccess) return e;
     smem_set.fetch_or(bit, std::memory_order_acq_rel);
   }
+  args.units = args.G * args.x_tiles * args.y_tiles * args.splits;
+  args.persistent = args.splits == 1 ? 1 : 0;
+  const int grid = args.persistent ? (args.units < num_sms ? args.units : num_sms) : args.units;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(args.x_tiles * args.y_tiles * args.splits), (unsigned)args.G, 1);
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  cfg.numAttrs = 0;
+  // Programmatic dependent launch: the grid may start while the preceding
+  // kernel on the stream finishes; it waits (griddepcontrol.wait) before
+  // reading anything that kernel produced.
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (args.splits > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)args.splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)args.splits;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
   }
   return cudaLaunchKernelEx(&cfg, kern, tm_act, tm_w, args);
 }
@@ -426,7 +800,7 @@ cudaError_t launch_cfg(const uint8_t* a, const uint8_t* w, BmmArgs args, cudaStr
 cudaError_t launch_bmm_a8w8(const uint8_t* a, const uint8_t* a_sf, const uint8_t* w,
                             const uint8_t* w_sf, void* out, int64_t T, int G, int N, int K,
                             int num_sms, cudaStream_t s, const char** why) {
-  BmmArgs args;
+  BmmArgs args = {};
   args.a_sf = a_sf;
   args.w_sf = w_sf;
   args.out = reinterpret_cast<__nv_bfloat16*>(out);
@@ -448,17 +822,50 @@ cudaError_t launch_bmm_a8w8(const uint8_t* a, const uint8_t* a_sf, const uint8_t
     args.kg_per_split = (int)ceil_div(args.KG, splits);
     args.splits = (int)ceil_div(args.KG, args.kg_per_split);
     switch (bn) {
-      case 16: return launch_cfg<true, 16, 10>(a, w, args, s, why);
-      case 32: return launch_cfg<true, 32, 10>(a, w, args, s, why);
-      case 64: return launch_cfg<true, 64, 8>(a, w, args, s, why);
-      default: return launch_cfg<true, 128, 6>(a, w, args, s, why);
+      case 16: return launch_cfg<true, false, 16, 10>(a, w, args, num_sms, s, why);
+      case 32: return launch_cfg<true, false, 32, 9>(a, w, args, num_sms, s, why);
+      case 64: return launch_cfg<true, false, 64, 8>(a, w, args, num_sms, s, why);
+      default: return launch_cfg<true, false, 128, 6>(a, w, args, num_sms, s, why);
     }
   }
   args.x_tiles = (int)ceil_div(T, 128);
   args.y_tiles = (int)ceil_div(N, 256);
   args.splits = 1;
   args.kg_per_split = args.KG;
-  return launch_cfg<false, 256, 4>(a, w, args, s, why);
+  return launch_cfg<false, false, 256, 4>(a, w, args, num_sms, s, why);
+}
+
+cudaError_t launch_wo_a_fused(const void* x, const int64_t* pos, const void* cos, const void* sin,
+                              int64_t cs_ld, int64_t max_pos, int R, const uint8_t* w,
+                              const uint8_t* w_sf, void* out, int64_t T, int G, int N, int K,
+                              int32_t* err_flag, int num_sms, cudaStream_t s, const char** why) {
+  BmmArgs args = {};
+  args.w_sf = w_sf;
+  args.out = reinterpret_cast<__nv_bfloat16*>(out);
+  args.T = (int)T;
+  args.G = G;
+  args.N = N;
+  args.K = K;
+  args.KG = (int)ceil_div(K, kGroup);
+  args.NB = (int)sf_row_blocks(N);
+  args.pos = pos;
+  args.cos_tab = reinterpret_cast<const uint16_t*>(cos);
+  args.sin_tab = reinterpret_cast<const uint16_t*>(sin);
+  args.cs_ld = cs_ld;
+  args.max_pos = max_pos;
+  args.R = R;
+  args.err_flag = err_flag;
+  args.x_tiles = (int)ceil_div(N, 128);
+  args.y_tiles = 1;
+  const int base = args.x_tiles * G;
+  int splits = num_sms / (base > 0 ? base : 1);
+  splits = splits < 1 ? 1 : (splits > 8 ? 8 : splits);
+  splits = splits > args.KG ? args.KG : splits;
+  args.kg_per_split = (int)ceil_div(args.KG, splits);
+  args.splits = (int)ceil_div(args.KG, args.kg_per_split);
+  if (T <= 16) return launch_cfg<true, true, 16, 9>(x, w, args, num_sms, s, why);
+  if (T <= 32) return launch_cfg<true, true, 32, 7>(x, w, args, num_sms, s, why);
+  return launch_cfg<true, true, 64, 5>(x, w, args, num_sms, s, why);
 }
 
 cudaError_t watchdog_read(uint32_t* value, bool clear) {
@@ -468,6 +875,11 @@ cudaError_t watchdog_read(uint32_t* value, bool clear) {
     e = cudaMemcpyToSymbol(g_watchdog, &zero, sizeof(uint32_t));
   }
   return e;
+}
+
+cudaError_t launch_watchdog_selftest(uint64_t limit_ns, cudaStream_t s) {
+  watchdog_selftest_kernel<<<1, 32, 0, s>>>(limit_ns);
+  return cudaGetLastError();
 }
 
 }  // namespace mxq

@@ -38,7 +38,19 @@ cudaError_t launch_bmm_a8w8(const uint8_t* a, const uint8_t* a_sf, const uint8_t
                             const uint8_t* w_sf, void* out, int64_t T, int G, int N, int K,
                             int num_sms, cudaStream_t s, const char** why);
 
+// One-launch wo_a / MXFP8 linear for T <= 64 tokens: the GEMM reads the BF16
+// activation and quantises it itself (inverse RoPE when R > 0).
+constexpr int kFusedMaxTokens = 64;
+cudaError_t launch_wo_a_fused(const void* x, const int64_t* pos, const void* cos, const void* sin,
+                              int64_t cs_ld, int64_t max_pos, int R, const uint8_t* w,
+                              const uint8_t* w_sf, void* out, int64_t T, int G, int N, int K,
+                              int32_t* err_flag, int num_sms, cudaStream_t s, const char** why);
+
 cudaError_t watchdog_read(uint32_t* value, bool clear);
+
+// One tiny kernel whose only wait can never be satisfied; it must give up
+// after limit_ns and set bit 31 of the watchdog word.
+cudaError_t launch_watchdog_selftest(uint64_t limit_ns, cudaStream_t s);
 
 // Stores `text` as the calling thread's last-error text (mxq_last_error) and
 // returns `status`.

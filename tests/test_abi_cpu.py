@@ -103,13 +103,36 @@ def test_bmm_argument_errors(L):
 
 
 def test_linear_argument_errors(L):
-    need = L.mxq_linear_workspace_bytes(8, 5120, 576)
-    assert need == 8 * 576 + 256 + 0  # codes (4608 B, 256-aligned) + 8*5 scale bytes -> 256
-    assert L.mxq_linear(P, P, P, P, 8, 5120, 576, None, 0, None) == 6
-    assert L.mxq_linear(P, P, P, P, 8, 5120, 576, P, need - 1, None) == 6
+    assert L.mxq_linear_workspace_bytes(8, 5120, 576) == 0  # <= 64 rows: one fused launch
+    need = L.mxq_linear_workspace_bytes(100, 5120, 576)
+    assert need == 100 * 576 + 512  # codes (57600 B, 256-aligned) + 100*5 scale bytes -> 512
+    assert L.mxq_linear(P, P, P, P, 100, 5120, 576, None, 0, None) == 6
+    assert L.mxq_linear(P, P, P, P, 100, 5120, 576, P, need - 1, None) == 6
     assert L.mxq_linear(None, P, P, P, 8, 5120, 576, P, need, None) == 1
     assert L.mxq_linear(P, P, P, P, 8, 5120, 570, P, need, None) == 2
     assert L.mxq_linear(P, P, P, P, 0, 5120, 576, None, 0, None) == 0
+
+
+def wo_a(L, x=P, pos=P, cos=P, sin=P, cs_ld=32, max_pos=16, w=P, wsf=P, out=P, T=4, G=8, D=4096,
+         N=1024, R=64, err=None, ws=None, ws_bytes=0):
+    return L.mxq_wo_a(x, pos, cos, sin, cs_ld, max_pos, w, wsf, out, T, G, D, N, R, err, ws,
+                      ws_bytes, None)
+
+
+def test_wo_a_argument_errors(L):
+    assert wo_a(L, x=None) == 1
+    assert wo_a(L, pos=None) == 1
+    assert wo_a(L, wsf=None) == 1
+    assert wo_a(L, D=4100) == 2
+    assert wo_a(L, N=1000) == 2
+    assert wo_a(L, R=8) == 4
+    assert wo_a(L, D=4160, R=64) == 4
+    assert wo_a(L, cs_ld=36) == 3
+    assert wo_a(L, out=U) == 3
+    assert wo_a(L, T=0, x=None, out=None) == 0
+    assert L.mxq_wo_a_workspace_bytes(64, 8, 4096, 1024) == 0
+    assert L.mxq_wo_a_workspace_bytes(8192, 8, 4096, 1024) == 8192 * 8 * 4096 + 8192 * 8 * 32
+    assert wo_a(L, T=8192) == 6  # prefill sizes go through the workspace
 
 
 def test_dequant_and_scale_argument_errors(L):

@@ -1,0 +1,99 @@
+"""GPU parity of mxq_wo_a, the whole wo_a projection in one call (one fused
+launch for T <= 64, quantiser + GEMM through a workspace above), against the
+oracle: inverse RoPE + group quantisation, then the block-scaled GEMM."""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from cases import check_gemm, oracle_quant, oracle_weights, to_dev, wo_a_inputs
+from oracle import mx_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mxq():
+    import mxfp8_block_scaled_inv_gb300 as m
+    from mxfp8_block_scaled_inv_gb300 import build
+
+    build.build()
+    m.lib()
+    m.mxq_watchdog_read(clear=True)
+    yield m
+    assert m.mxq_watchdog_read() == 0
+
+
+def run(mxq, x, pos, cos, sin, w, sw, R, err=None):
+    D = x.shape[-1]
+    xd, pd, cd, sd, wd, swd = to_dev(x, pos, cos, sin, w, sw)
+    wsf = mxq.mxq_prepare_weight_scales(swd, D)
+    out = mxq.mxq_wo_a(xd, pd, cd, sd, wd, wsf, R=R, err_flag=err)
+    torch.cuda.synchronize()
+    return out, (xd, pd, cd, sd, wd, wsf)
+
+
+@pytest.mark.parametrize("T", [1, 8, 32, 64])
+def test_decode_shapes_one_launch(mxq, T):
+    """x [T, 8, 4096] at random positions in [0, 32768), W [8, 1024, 4096]."""
+    x, pos, cos, sin = wo_a_inputs(T, 8, 4096, 1024, 64, seed=1300 + T, max_pos_table=32768)
+    w, sw = oracle_weights(8, 1024, 4096, seed=3)
+    out, _ = run(mxq, x, pos, cos, sin, w, sw, 64)
+    a, sa = oracle_quant(x, pos, cos, sin, 64)
+    check_gemm(out, *O.bmm_a8w8_ref(a, sa, w, sw), f"wo_a T={T}")
+
+
+@pytest.mark.parametrize("R", [0, 16, 32, 64, 128])
+@pytest.mark.parametrize("T", [3, 17, 33, 63])
+def test_ragged_tokens_and_rope_widths(mxq, T, R):
+    x, pos, cos, sin = wo_a_inputs(T, 2, 512, 256, max(R, 16), seed=1400 + T + R, max_pos=5000)
+    w, sw = oracle_weights(2, 256, 512, seed=1401)
+    out, _ = run(mxq, x, pos, cos, sin, w, sw, R)
+    a, sa = oracle_quant(x, pos, cos, sin, R)
+    check_gemm(out, *O.bmm_a8w8_ref(a, sa, w, sw), f"T={T} R={R}")
+
+
+@pytest.mark.parametrize("T", [65, 100, 300])
+def test_larger_token_counts_use_two_kernels(mxq, T):
+    x, pos, cos, sin = wo_a_inputs(T, 2, 1024, 256, 64, seed=1500 + T, max_pos=4096)
+    w, sw = oracle_weights(2, 256, 1024, seed=1501)
+    out, _ = run(mxq, x, pos, cos, sin, w, sw, 64)
+    a, sa = oracle_quant(x, pos, cos, sin, 64)
+    check_gemm(out, *O.bmm_a8w8_ref(a, sa, w, sw), f"T={T}")
+
+
+@pytest.mark.parametrize("D", [288, 576, 2304])
+def test_unaligned_k_without_rope(mxq, D):
+    x, pos, cos, sin = wo_a_inputs(8, 2, D, 512, 16, seed=1600 + D, max_pos=64)
+    w, sw = oracle_weights(2, 512, D, seed=1601 + D)
+    out, _ = run(mxq, x, pos, cos, sin, w, sw, 0)
+    a, sa = oracle_quant(x, pos, cos, sin, 0)
+    check_gemm(out, *O.bmm_a8w8_ref(a, sa, w, sw), f"D={D}")
+
+
+@pytest.mark.parametrize("T", [1, 8, 64])
+def test_one_launch_equals_two_calls(mxq, T):
+    """The fused launch and the quantiser + GEMM sequence give identical bytes."""
+    x, pos, cos, sin = wo_a_inputs(T, 8, 4096, 1024, 64, seed=1700 + T, max_pos_table=32768)
+    w, sw = oracle_weights(8, 1024, 4096, seed=3)
+    out, (xd, pd, cd, sd, wd, wsf) = run(mxq, x, pos, cos, sin, w, sw, 64)
+    q, sc = mxq.mxq_inv_rope_group_quant(xd, pd, cd, sd, 64)
+    out2 = mxq.mxq_bmm_a8w8(q, sc, wd, wsf)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2)
+
+
+def test_out_of_range_position_in_one_launch(mxq):
+    T = 6
+    x, _, cos, sin = wo_a_inputs(T, 2, 256, 128, 64, seed=1800, max_pos=100, max_pos_table=100)
+    pos = torch.tensor([3, -1, 50, 100, 99, 7], dtype=torch.int64)
+    w, sw = oracle_weights(2, 128, 256, seed=1801)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, _ = run(mxq, x, pos, cos, sin, w, sw, 64, err=err)
+    assert int(err.item()) == mxq.MXQ_DEVERR_POSITION
+    o = out.float().cpu()
+    assert (o[1] == 0).all() and (o[3] == 0).all()
+    good = np.array([0, 2, 4, 5])
+    a, sa = oracle_quant(x[good], pos[good], cos, sin, 64)
+    check_gemm(out[good], *O.bmm_a8w8_ref(a, sa, w, sw), "good rows")
