@@ -156,7 +156,7 @@ int mxq_bmm_a8w8(const uint8_t* a_e4m3, const uint8_t* a_e8m0, const uint8_t* w_
                  const uint8_t* w_sf_prepared, void* out_bf16, int64_t T, int32_t G, int32_t N,
                  int32_t K, void* ws, size_t ws_bytes, mxq_stream_t stream);
 
-/* Workspace bytes mxq_linear needs: 0 for M <= 64 (one fused launch),
+/* Workspace bytes mxq_linear needs: 0 for M <= 32 (one fused launch),
  * otherwise the quantised activation codes and scales plus the GEMM
  * workspace. */
 size_t mxq_linear_workspace_bytes(int64_t M, int32_t N, int32_t K);
@@ -167,7 +167,7 @@ size_t mxq_linear_workspace_bytes(int64_t M, int32_t N, int32_t K);
  * (dequantise-once page, Purpose: K = 576 at TP4, 288 at TP8).  x is BF16;
  * it is quantised per row in groups of 128 exactly as
  * mxq_inv_rope_group_quant with R = 0 and multiplied as mxq_bmm_a8w8 with
- * G = 1: for M <= 64 in one launch that quantises inside the GEMM, else
+ * G = 1: for M <= 32 in one launch that quantises inside the GEMM, else
  * through the workspace.  w_sf_prepared from
  * mxq_prepare_weight_scales(.., B=1, N, K).  M == 0 is a no-op.
  */
@@ -175,7 +175,7 @@ int mxq_linear(const void* x_bf16, const uint8_t* w_e4m3, const uint8_t* w_sf_pr
                void* out_bf16, int64_t M, int32_t N, int32_t K, void* ws, size_t ws_bytes,
                mxq_stream_t stream);
 
-/* Workspace bytes mxq_wo_a needs: 0 for T <= 64, else T*G*D code bytes and
+/* Workspace bytes mxq_wo_a needs: 0 for T <= 32, else T*G*D code bytes and
  * T*G*ceil(D/128) scale bytes (each rounded up to 256). */
 size_t mxq_wo_a_workspace_bytes(int64_t T, int32_t G, int32_t D, int32_t N);
 
@@ -185,7 +185,7 @@ size_t mxq_wo_a_workspace_bytes(int64_t T, int32_t G, int32_t D, int32_t N);
  * rules and results (codes and scales bit-identical; the output equal to
  * the two-call sequence).  FP8 WO_A page, Summary items 1-2.
  *
- * For T <= 64 tokens (decode) it is ONE launch: the GEMM reads the BF16 x
+ * For T <= 32 tokens (decode) it is ONE launch: the GEMM reads the BF16 x
  * and quantises each tile itself, so neither the codes nor a second launch
  * cost anything (this goes beyond the pages' two-kernel design).  For larger
  * T the codes go through `ws` (mxq_wo_a_workspace_bytes) and two kernels run.

@@ -244,7 +244,7 @@ def mxq_wo_a_workspace_bytes(T, G, D, N):
 
 def mxq_wo_a(x, pos, cos, sin, w, w_sf, R=64, out=None, ws=None, err_flag=None, stream=None):
     """The wo_a projection in one library call: x bf16 [T, G, D] -> out bf16 [T, G, N]
-    (one fused launch for T <= 64; quantiser + GEMM through `ws` otherwise)."""
+    (one fused launch for T <= 32; quantiser + GEMM through `ws` otherwise)."""
     T, G, D = x.shape
     N = w.shape[1]
     if out is None:

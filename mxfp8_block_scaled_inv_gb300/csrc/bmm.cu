@@ -40,7 +40,7 @@
 //           thread-block cluster, whose fp32 partial tiles are summed in rank
 //           order through distributed shared memory (deterministic, no global
 //           workspace).
-// Fused activation form (swapped orientation, T <= 64): the activation is
+// Fused activation form (swapped orientation, T <= 32): the activation is
 // read as BF16 straight from the attention output by TMA, and the epilogue
 // warps, idle during the mainloop, quantise each stage's tokens (inverse
 // RoPE on the last group, group-128 E8M0 scale, E4M3 codes) directly into
@@ -73,7 +73,6 @@ constexpr uint32_t kWdProducer = 1, kWdMma = 2, kWdEpilogue = 4, kWdDrain = 8, k
 constexpr int kWarps = 11;
 constexpr int kThreads = kWarps * 32;
 constexpr int kEpiWarp0 = 3;
-constexpr int kSfChunk = 64;  // K groups held by one compact activation-scale buffer
 
 struct BmmArgs {
   const uint8_t* a_sf;  // [T][G][KG]
@@ -104,7 +103,10 @@ struct Cfg {
   static constexpr int SFX_BYTES = kSfAtomBytes;
   static constexpr int SFY_BYTES = Y_ATOMS * kSfAtomBytes;
   static constexpr int W_SF_BYTES = (SWAP ? 1 : Y_ATOMS) * kSfAtomBytes;
-  static constexpr int CSF_BYTES = FUSED ? 0 : kSfChunk * 128;  // [group][128 rows]
+  // Compact activation-scale buffer: groups per chunk (a few-token CTA
+  // holds only a short K slice, so its chunks are smaller).
+  static constexpr int SF_CHUNK = SWAP ? 16 : 64;
+  static constexpr int CSF_BYTES = FUSED ? 0 : SF_CHUNK * 128;  // [group][128 rows]
   static constexpr int STG_BYTES = FUSED ? BN * 256 : 0;         // BF16 staging [BN][128]
   static constexpr int OFF_X = 0;
   static constexpr int OFF_Y = OFF_X + NSTAGE * X_TILE;
@@ -112,12 +114,22 @@ struct Cfg {
   static constexpr int OFF_SFY = OFF_SFX + NSTAGE * SFX_BYTES;
   static constexpr int OFF_STG = OFF_SFY + NSTAGE * SFY_BYTES;
   static constexpr int OFF_CSF = OFF_STG + NSTAGE * STG_BYTES;
-  static constexpr int OFF_BAR = OFF_CSF + 2 * CSF_BYTES;
+  // fp32 split-K receive buffer of the swapped form: [split][rows owned][BN+4]
+  // with rows owned = ceil(128 / splits); splits * that <= 133 for splits <= 8.
+  static constexpr int PART_PITCH = BN + 4;
+  static constexpr int RED_ROWS = 136;
+  static constexpr int RED_BYTES = SWAP ? RED_ROWS * PART_PITCH * 4 : 0;
+  static constexpr int OFF_RED = OFF_CSF + 2 * CSF_BYTES;
+  static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
   // full[NSTAGE], empty[NSTAGE], landed[NSTAGE], acc_full, acc_empty,
   // sf_full[2], sf_empty[2], mma_done
   static constexpr int N_BARS = 3 * NSTAGE + 7;
   static constexpr int OFF_SLOT = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_SLOT + 16 + 1024;
+  // Two CTAs share an SM when their shared memory allows it (the small-token
+  // forms): more K slices stream at once, and with programmatic dependent
+  // launch the next call's CTAs start streaming weights beside this one's.
+  static constexpr int CTAS_PER_SM = SMEM_BYTES <= 113 * 1024 ? 2 : 1;
   static constexpr int SF_COLS = 4 + 4 * Y_ATOMS;
   static constexpr int TMEM_USED = BN + NSTAGE * SF_COLS;
   static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
@@ -126,7 +138,6 @@ struct Cfg {
                                    : TMEM_USED <= 256 ? 256
                                                       : 512;
   static constexpr int HALF = BN / 2;        // columns drained by one epilogue warp
-  static constexpr int PART_PITCH = BN + 1;  // fp32 partial tile [128][BN+1] (aliases stages)
   // Instruction descriptor, kind::mxf8f6f4 with block scaling: E4M3 A and
   // B (format 0), both K-major, N >> 3 at bits 17-22, UE8M0 scale type at
   // bit 23, M >> 4 at bits 24-28, scale-factor ids 0.
@@ -134,8 +145,7 @@ struct Cfg {
       (1u << 23) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(128 * PART_PITCH * 4 <= OFF_SFX, "partial tile must fit in the operand buffers");
-  static_assert(!FUSED || (SWAP && BN <= 64), "fused activations: swapped form, <= 64 tokens");
+  static_assert(!FUSED || (SWAP && BN <= 32), "fused activations: swapped form, <= 32 tokens");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
   static_assert(ACT_ROWS <= 128, "activation scale rows fit one loader pass");
   static_assert(HALF % 8 == 0, "epilogue drains 8-column chunks");
@@ -182,7 +192,7 @@ __device__ __forceinline__ Unit decode_unit(const BmmArgs& p, int u) {
 }
 
 template <bool SWAP, bool FUSED, int BN, int NSTAGE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, (Cfg<SWAP, FUSED, BN, NSTAGE>::CTAS_PER_SM))
     bmm_a8w8_kernel(const __grid_constant__ CUtensorMap tm_act,
                     const __grid_constant__ CUtensorMap tm_w, const BmmArgs p) {
   using C = Cfg<SWAP, FUSED, BN, NSTAGE>;
@@ -238,6 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The next kernel on the stream may be scheduled now: it only streams its
+  // own weights until it has waited for this grid to complete.
+  if (threadIdx.x == 0) ptx::griddep_launch_dependents();
 
   if (warp == 0) {
     if constexpr (FUSED) {
@@ -340,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) issue_weights(w, s, kg);
           ++issued;
         }
-        if ((kk % kSfChunk) == 0 &&
+        if ((kk % C::SF_CHUNK) == 0 &&
             !ptx::mbar_wait(&sf_full[b], (uint32_t)(ci >> 1) & 1u, kWaitLimitNs)) {
           watchdog(abort_flag, kWdProducer);
           stop = true;
@@ -353,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Activation-scale atom: lane i writes the 16-byte line of rows
         // i, i+32, i+64, i+96 (one word each, the byte replicated four times).
-        const uint8_t* col = csf + b * C::CSF_BYTES + (kk % kSfChunk) * 128;
+        const uint8_t* col = csf + b * C::CSF_BYTES + (kk % C::SF_CHUNK) * 128;
         uint4 line;
         line.x = (uint32_t)col[lane] * 0x01010101u;
         line.y = (uint32_t)col[lane + 32] * 0x01010101u;
@@ -365,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&full[s]);
         ++it;
-        if ((kk % kSfChunk) == kSfChunk - 1 || kk == w.nk - 1) {
+        if ((kk % C::SF_CHUNK) == C::SF_CHUNK - 1 || kk == w.nk - 1) {
           if (lane == 0) ptx::mbar_arrive(&sf_empty[b]);
           ++ci;
         }
@@ -447,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Unit w = decode_unit<SWAP, BN>(p, u);
       const int row0 = SWAP ? w.y0 : w.x0;
       if (u == u_first) ptx::griddep_wait();  // the scales come from the preceding kernel
-      for (int c0 = 0; c0 < w.nk; c0 += kSfChunk) {
+      for (int c0 = 0; c0 < w.nk; c0 += C::SF_CHUNK) {
         const int b = ci & 1;
         if (*abort_flag ||
             !ptx::mbar_wait(&sf_empty[b], ((uint32_t)(ci >> 1) & 1u) ^ 1u, kWaitLimitNs)) {
@@ -455,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           stop = true;
           break;
         }
-        const int ng = min(kSfChunk, w.nk - c0);
+        const int ng = min(C::SF_CHUNK, w.nk - c0);
         const int kg0 = w.kg_begin + c0;
         uint8_t* dst = csf + b * C::CSF_BYTES;
 #pragma unroll
@@ -466,12 +479,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint8_t* src = p.a_sf + ((size_t)(valid ? t : 0) * p.G + w.g) * p.KG + kg0;
           if (valid && ((p.KG | kg0 | ng) & 15) == 0) {
             // 16-byte vectors: the row start and the chunk are 16-byte aligned.
-            uint4 v[kSfChunk / 16];
+            uint4 v[C::SF_CHUNK / 16];
 #pragma unroll
-            for (int q = 0; q < kSfChunk / 16; ++q)
+            for (int q = 0; q < C::SF_CHUNK / 16; ++q)
               if (q * 16 < ng) v[q] = __ldg(reinterpret_cast<const uint4*>(src) + q);
 #pragma unroll
-            for (int q = 0; q < kSfChunk / 16; ++q) {
+            for (int q = 0; q < C::SF_CHUNK / 16; ++q) {
               if (q * 16 >= ng) break;
               const uint32_t wv[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
 #pragma unroll
@@ -495,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = (warp - kEpiWarp0) >> 2;        // which half of the columns
     const int r = q * 32 + lane;                  // accumulator row (TMEM lane)
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + h * C::HALF;
-    float* part = reinterpret_cast<float*>(smem);  // split-K partial tile (stage buffers idle)
+    float* red = reinterpret_cast<float*>(smem + C::OFF_RED);  // split-K receive buffer
     int ti = 0;
     int itq = 0;  // stage counter of the fused activation quantisation
     if constexpr (FUSED) {
@@ -655,39 +668,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             p.out[((size_t)t * p.G + w.g) * p.N + n] = __float2bfloat16_rn(__uint_as_float(v[j]));
         }
       } else {
+        // Split K: push this row's fp32 partial straight into the receive
+        // buffer of the cluster CTA that owns the row (slot = our rank).
+        const int rps = (C::BM + p.splits - 1) / p.splits;
+        const int owner = r / rps;
+        const uint32_t dst = ptx::map_shared_rank(
+            ptx::smem_u32(red + ((w.split * rps + (r - owner * rps)) * C::PART_PITCH + c0)),
+            (uint32_t)owner);
 #pragma unroll
-        for (int j = 0; j < C::HALF; ++j) part[r * C::PART_PITCH + c0 + j] = __uint_as_float(v[j]);
+        for (int j = 0; j < C::HALF; j += 4)
+          ptx::st_shared_cluster_f32x4(dst + j * 4, __uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                       __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
       }
     }
   }
 
   __syncthreads();
   if (SWAP && p.splits > 1) {
-    // Deterministic split-K reduction over the cluster (one unit per CTA):
-    // CTA `split` sums rows [split*rows, (split+1)*rows) of the tile over the
-    // ranks 0..splits-1 in order.
+    // Deterministic split-K reduction over the cluster (one unit per CTA).
+    // Every CTA pushed its partial rows to their owners before the barrier;
+    // after it, CTA `split` sums the rows it owns over ranks 0..splits-1 in
+    // order, from its own shared memory, and nobody touches a peer again.
     const Unit w = decode_unit<SWAP, BN>(p, u_first);
     ptx::cluster_sync();
-    const int rows = (C::BM + p.splits - 1) / p.splits;
-    const int r_begin = w.split * rows;
-    const int r_end = min(C::BM, r_begin + rows);
+    const int rps = (C::BM + p.splits - 1) / p.splits;
+    const int r_begin = w.split * rps;
+    const int nrows = min(C::BM, r_begin + rps) - r_begin;
     const int tv = min(BN, p.T - w.y0);
-    const int nrows = r_end - r_begin;
     if (!*abort_flag && nrows > 0 && tv > 0) {
-      const uint32_t part0 = ptx::smem_u32(smem);
-      for (int e = threadIdx.x; e < nrows * tv; e += kThreads) {
-        const int tl = e / nrows;
-        const int rr = r_begin + e % nrows;
-        const uint32_t off = (uint32_t)(rr * C::PART_PITCH + tl) * 4u;
-        float acc = 0.0f;
-        for (int rk = 0; rk < p.splits; ++rk)
-          acc += ptx::ld_shared_cluster_f32(ptx::map_shared_rank(part0 + off, (uint32_t)rk));
-        const int n = w.x0 + rr;
-        if (n < p.N)
-          p.out[((size_t)(w.y0 + tl) * p.G + w.g) * p.N + n] = __float2bfloat16_rn(acc);
+      // Work item = (row, 4 consecutive tokens), rows fastest so that the
+      // BF16 stores of a warp are contiguous along n.
+      const float* red = reinterpret_cast<const float*>(smem + C::OFF_RED);
+      const int tv4 = (tv + 3) >> 2;
+      for (int e = threadIdx.x; e < nrows * tv4; e += kThreads) {
+        const int tl = (e / nrows) * 4;
+        const int rr = e % nrows;
+        float4 acc = *reinterpret_cast<const float4*>(red + rr * C::PART_PITCH + tl);
+        for (int rk = 1; rk < p.splits; ++rk) {
+          const float4 pv =
+              *reinterpret_cast<const float4*>(red + (rk * rps + rr) * C::PART_PITCH + tl);
+          acc.x += pv.x;
+          acc.y += pv.y;
+          acc.z += pv.z;
+          acc.w += pv.w;
+        }
+        const int n = w.x0 + r_begin + rr;
+        if (n < p.N) {
+          const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+          __nv_bfloat16* o = p.out + ((size_t)(w.y0 + tl) * p.G + w.g) * p.N + n;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (tl + j < tv) o[(size_t)j * p.G * p.N] = __float2bfloat16_rn(a4[j]);
+        }
       }
     }
-    ptx::cluster_sync();  // keep every partial tile alive until all readers are done
   }
   if (warp == 1) {
     ptx::tc_fence_after();
@@ -769,9 +803,24 @@ cudaError_t launch_cfg(const void* a, const uint8_t* w, BmmArgs args, int num_sm
     if (e != cudaSuccess) return e;
     smem_set.fetch_or(bit, std::memory_order_acq_rel);
   }
+  if (SWAP) {
+    // Split K so that about one wave of CTAs streams the weights (deterministic
+    // rank-order reduction over a cluster of at most 8).
+    const int base = args.x_tiles * args.y_tiles * args.G;
+    int splits = (num_sms * C::CTAS_PER_SM) / (base > 0 ? base : 1);
+    splits = splits < 1 ? 1 : (splits > 8 ? 8 : splits);
+    splits = splits > args.KG ? args.KG : splits;
+    args.kg_per_split = (int)ceil_div(args.KG, splits);
+    args.splits = (int)ceil_div(args.KG, args.kg_per_split);
+    if (args.splits > 1 && args.splits * (int)ceil_div(C::BM, args.splits) > C::RED_ROWS) {
+      *why = "split-K receive buffer too small for this split count";
+      return cudaErrorInvalidValue;
+    }
+  }
   args.units = args.G * args.x_tiles * args.y_tiles * args.splits;
   args.persistent = args.splits == 1 ? 1 : 0;
-  const int grid = args.persistent ? (args.units < num_sms ? args.units : num_sms) : args.units;
+  const int slots = num_sms * C::CTAS_PER_SM;
+  const int grid = args.persistent ? (args.units < slots ? args.units : slots) : args.units;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -812,21 +861,12 @@ cudaError_t launch_bmm_a8w8(const uint8_t* a, const uint8_t* a_sf, const uint8_t
   args.NB = (int)sf_row_blocks(N);
   if (T <= 128) {
     // Few tokens: weight rows on the MMA M axis, tokens on N.
-    const int bn = T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128;
     args.x_tiles = (int)ceil_div(N, 128);
     args.y_tiles = 1;
-    const int base = args.x_tiles * G;
-    int splits = num_sms / (base > 0 ? base : 1);
-    splits = splits < 1 ? 1 : (splits > 8 ? 8 : splits);
-    splits = splits > args.KG ? args.KG : splits;
-    args.kg_per_split = (int)ceil_div(args.KG, splits);
-    args.splits = (int)ceil_div(args.KG, args.kg_per_split);
-    switch (bn) {
-      case 16: return launch_cfg<true, false, 16, 10>(a, w, args, num_sms, s, why);
-      case 32: return launch_cfg<true, false, 32, 9>(a, w, args, num_sms, s, why);
-      case 64: return launch_cfg<true, false, 64, 8>(a, w, args, num_sms, s, why);
-      default: return launch_cfg<true, false, 128, 6>(a, w, args, num_sms, s, why);
-    }
+    if (T <= 16) return launch_cfg<true, false, 16, 5>(a, w, args, num_sms, s, why);
+    if (T <= 32) return launch_cfg<true, false, 32, 4>(a, w, args, num_sms, s, why);
+    if (T <= 64) return launch_cfg<true, false, 64, 6>(a, w, args, num_sms, s, why);
+    return launch_cfg<true, false, 128, 4>(a, w, args, num_sms, s, why);
   }
   args.x_tiles = (int)ceil_div(T, 128);
   args.y_tiles = (int)ceil_div(N, 256);
@@ -857,15 +897,8 @@ cudaError_t launch_wo_a_fused(const void* x, const int64_t* pos, const void* cos
   args.err_flag = err_flag;
   args.x_tiles = (int)ceil_div(N, 128);
   args.y_tiles = 1;
-  const int base = args.x_tiles * G;
-  int splits = num_sms / (base > 0 ? base : 1);
-  splits = splits < 1 ? 1 : (splits > 8 ? 8 : splits);
-  splits = splits > args.KG ? args.KG : splits;
-  args.kg_per_split = (int)ceil_div(args.KG, splits);
-  args.splits = (int)ceil_div(args.KG, args.kg_per_split);
-  if (T <= 16) return launch_cfg<true, true, 16, 9>(x, w, args, num_sms, s, why);
-  if (T <= 32) return launch_cfg<true, true, 32, 7>(x, w, args, num_sms, s, why);
-  return launch_cfg<true, true, 64, 5>(x, w, args, num_sms, s, why);
+  if (T <= 16) return launch_cfg<true, true, 16, 4>(x, w, args, num_sms, s, why);
+  return launch_cfg<true, true, 32, 3>(x, w, args, num_sms, s, why);
 }
 
 cudaError_t watchdog_read(uint32_t* value, bool clear) {

@@ -38,9 +38,11 @@ cudaError_t launch_bmm_a8w8(const uint8_t* a, const uint8_t* a_sf, const uint8_t
                             const uint8_t* w_sf, void* out, int64_t T, int G, int N, int K,
                             int num_sms, cudaStream_t s, const char** why);
 
-// One-launch wo_a / MXFP8 linear for T <= 64 tokens: the GEMM reads the BF16
-// activation and quantises it itself (inverse RoPE when R > 0).
-constexpr int kFusedMaxTokens = 64;
+// One-launch wo_a / MXFP8 linear for T <= 32 tokens: the GEMM reads the BF16
+// activation and quantises it itself (inverse RoPE when R > 0).  Above 32
+// tokens the per-stage quantisation inside the GEMM costs more than a
+// separate quantiser launch, so those calls use two kernels.
+constexpr int kFusedMaxTokens = 32;
 cudaError_t launch_wo_a_fused(const void* x, const int64_t* pos, const void* cos, const void* sin,
                               int64_t cs_ld, int64_t max_pos, int R, const uint8_t* w,
                               const uint8_t* w_sf, void* out, int64_t T, int G, int N, int K,

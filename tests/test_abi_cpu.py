@@ -103,7 +103,7 @@ def test_bmm_argument_errors(L):
 
 
 def test_linear_argument_errors(L):
-    assert L.mxq_linear_workspace_bytes(8, 5120, 576) == 0  # <= 64 rows: one fused launch
+    assert L.mxq_linear_workspace_bytes(8, 5120, 576) == 0  # <= 32 rows: one fused launch
     need = L.mxq_linear_workspace_bytes(100, 5120, 576)
     assert need == 100 * 576 + 512  # codes (57600 B, 256-aligned) + 100*5 scale bytes -> 512
     assert L.mxq_linear(P, P, P, P, 100, 5120, 576, None, 0, None) == 6
@@ -130,7 +130,8 @@ def test_wo_a_argument_errors(L):
     assert wo_a(L, cs_ld=36) == 3
     assert wo_a(L, out=U) == 3
     assert wo_a(L, T=0, x=None, out=None) == 0
-    assert L.mxq_wo_a_workspace_bytes(64, 8, 4096, 1024) == 0
+    assert L.mxq_wo_a_workspace_bytes(32, 8, 4096, 1024) == 0
+    assert L.mxq_wo_a_workspace_bytes(33, 8, 4096, 1024) == 33 * 8 * 4096 + 33 * 8 * 32
     assert L.mxq_wo_a_workspace_bytes(8192, 8, 4096, 1024) == 8192 * 8 * 4096 + 8192 * 8 * 32
     assert wo_a(L, T=8192) == 6  # prefill sizes go through the workspace
 

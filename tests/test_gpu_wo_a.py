@@ -1,5 +1,5 @@
 """GPU parity of mxq_wo_a, the whole wo_a projection in one call (one fused
-launch for T <= 64, quantiser + GEMM through a workspace above), against the
+launch for T <= 32, quantiser + GEMM through a workspace above), against the
 oracle: inverse RoPE + group quantisation, then the block-scaled GEMM."""
 
 import numpy as np
@@ -54,7 +54,7 @@ def test_ragged_tokens_and_rope_widths(mxq, T, R):
     check_gemm(out, *O.bmm_a8w8_ref(a, sa, w, sw), f"T={T} R={R}")
 
 
-@pytest.mark.parametrize("T", [65, 100, 300])
+@pytest.mark.parametrize("T", [33, 65, 100, 300])
 def test_larger_token_counts_use_two_kernels(mxq, T):
     x, pos, cos, sin = wo_a_inputs(T, 2, 1024, 256, 64, seed=1500 + T, max_pos=4096)
     w, sw = oracle_weights(2, 256, 1024, seed=1501)
@@ -72,16 +72,24 @@ def test_unaligned_k_without_rope(mxq, D):
     check_gemm(out, *O.bmm_a8w8_ref(a, sa, w, sw), f"D={D}")
 
 
-@pytest.mark.parametrize("T", [1, 8, 64])
-def test_one_launch_equals_two_calls(mxq, T):
-    """The fused launch and the quantiser + GEMM sequence give identical bytes."""
+@pytest.mark.parametrize("T", [1, 8, 32])
+def test_one_launch_matches_two_calls(mxq, T):
+    """The fused launch and the quantiser + GEMM sequence agree within the GEMM
+    tolerance (the two may split K differently, so fp32 sums can differ in the
+    last place; the quantised operands are the same)."""
     x, pos, cos, sin = wo_a_inputs(T, 8, 4096, 1024, 64, seed=1700 + T, max_pos_table=32768)
     w, sw = oracle_weights(8, 1024, 4096, seed=3)
     out, (xd, pd, cd, sd, wd, wsf) = run(mxq, x, pos, cos, sin, w, sw, 64)
     q, sc = mxq.mxq_inv_rope_group_quant(xd, pd, cd, sd, 64)
     out2 = mxq.mxq_bmm_a8w8(q, sc, wd, wsf)
     torch.cuda.synchronize()
-    assert torch.equal(out, out2)
+    a, sa = oracle_quant(x, pos, cos, sin, 64)
+    y_ref, S = O.bmm_a8w8_ref(a, sa, w, sw)
+    assert np.array_equal(q.cpu().numpy(), a) and np.array_equal(sc.cpu().numpy(), sa)
+    y1 = out.float().cpu().numpy().astype(np.float64)
+    y2 = out2.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(y1 - y2) <= O.gemm_tolerance(y2, S))
+    check_gemm(out, y_ref, S, "fused")
 
 
 def test_out_of_range_position_in_one_launch(mxq):
