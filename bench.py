@@ -414,6 +414,64 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def single_workload(mxq, device, peaks, args):
+    """Eager run of one secondary workload (decode layer or MXFP8 linear) over
+    24 distinct weight sets: --warmup passes, then --steps timed calls."""
+    import workloads as W
+
+    n_sets = 24
+    if args.workload == "decode":
+        T = args.tokens
+        wsets = make_weights(mxq, n_sets, seed=5000, device=device)
+        cos, sin = rope_tables(32768, device)
+        x = W.bf16_normal_cuda((T, G, D), seed=6000 + T, device=device)
+        pos = W.positions_uniform_cuda(T, seed=6100 + T, max_pos=32768, device=device)
+        o = torch.empty((T, G, N), dtype=torch.bfloat16, device=device)
+        need = mxq.mxq_wo_a_workspace_bytes(T, G, D, N)
+        ws = torch.empty(need, dtype=torch.uint8, device=device) if need else None
+
+        def call(i):
+            wq, wsf, _ = wsets[i % n_sets]
+            mxq.wo_a(x, pos, cos, sin, wq, wsf, R=R, out=o, ws=ws)
+
+        byt = G * N * D + G * N * KG + T * (2 * G * D + 8 + 2 * (R // 2) * 2) + 2 * T * G * N
+        desc = f"wo_a decode x [{T},8,4096] -> [{T},8,1024], W [8,1024,4096], {n_sets} weight sets"
+    else:
+        M, K, Nl = args.tokens, args.k, W.LINEAR_N
+        kg = (K + 127) // 128
+        sets = []
+        for i in range(n_sets):
+            wf = W.f32_normal_cuda((Nl, 1, K), seed=7000 + i, std=0.02, device=device)
+            wq, wsc = mxq.mxq_inv_rope_group_quant(wf.to(torch.bfloat16), R=0)
+            sets.append((wq.view(Nl, K), mxq.mxq_prepare_weight_scales(wsc.view(1, Nl, kg), K)))
+        x = W.bf16_normal_cuda((M, K), seed=7100 + M, device=device)
+        o = torch.empty((M, Nl), dtype=torch.bfloat16, device=device)
+        need = mxq.mxq_linear_workspace_bytes(M, Nl, K)
+        ws = torch.empty(need, dtype=torch.uint8, device=device) if need else None
+
+        def call(i):
+            wq, wsf = sets[i % n_sets]
+            mxq.mxq_linear(x, wq, wsf, out=o, ws=ws)
+
+        byt = Nl * K + Nl * kg + 2 * M * K + 2 * M * Nl
+        desc = f"MXFP8 linear x [{M},{K}] -> [{M},{Nl}], {n_sets} weight sets"
+    for i in range(max(args.warmup, 1) * n_sets):
+        call(i)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(args.steps):
+        call(i)
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / args.steps
+    if mxq.mxq_watchdog_read() != 0:
+        raise SystemExit("a bounded wait inside a kernel ran out")
+    return {"workload": args.workload, "config": desc, "steps": args.steps, "us_per_call": round(us, 3),
+            "gbs": round(byt / (us * 1e-6) / 1e9, 1),
+            "hbm_frac": round(byt / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4), "timing": "eager, back to back"}
+
+
 # ------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -423,6 +481,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--workload", choices=["prefill", "decode", "linear"], default="prefill",
+                    help="prefill (default, the headline); decode / linear: a short eager run "
+                         "of that workload alone (for profiling), its own JSON line")
+    ap.add_argument("--tokens", type=int, default=1, help="T (decode) or M (linear)")
+    ap.add_argument("--k", type=int, default=576, help="K of the linear workload")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -453,6 +516,10 @@ def main():
     mxq.lib()
     peaks = load_peaks()
     torch.manual_seed(0)
+    if args.workload != "prefill":
+        if rank == 0:
+            print(json.dumps(single_workload(mxq, device, peaks, args)), flush=True)
+        return
 
     # Inputs resident in HBM.  Each rank owns its own chunk (weak scaling, no exchange).
     x = W.bf16_normal_cuda((T_PREFILL, G, D), seed=400 + rank, outlier_frac=0.01, device=device)
