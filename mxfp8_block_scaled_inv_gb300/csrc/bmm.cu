@@ -9,13 +9,12 @@
 //   out[t, g, n] = bf16( sum_k A[t,g,k] * W[g,n,k] ),
 //   A = E4M3(a) * 2^(sa-127), W = E4M3(w) * 2^(sw-127), one scale per 128 k.
 //
-// Work unit = one 128 x BN output tile of one group g (and, for the split-K
-// form, one K slice of it).  Warp roles (11 warps):
-//   warp 0      producer: per pipeline stage (one 128-wide K group) TMA loads
-//               of the A and W tiles (128-byte swizzle, zero fill outside the
-//               tensor: this is the unaligned-K tail), a bulk copy of the
-//               prepared weight-scale atom(s), and the activation-scale atom
-//               built from the compact scale buffer in shared memory.
+// Work unit = one output tile of one group g (and, for the split-K form, one
+// K slice of it).  Warp roles (12 warps; 11 in the fused form):
+//   warp 0      weight producer: per pipeline stage (one 128-wide K group) a
+//               TMA load of the W tile (128-byte swizzle, zero fill outside
+//               the tensor: this is the unaligned-K tail) and a copy of the
+//               prepared weight-scale atom(s).
 //   warp 1      TMEM owner and MMA issuer: per stage, tcgen05.cp of the scale
 //               atoms into TMEM, four tcgen05.mma kind::mxf8f6f4 block_scale
 //               (K = 32 each; every word of an atom holds its group's byte four
@@ -24,29 +23,36 @@
 //               accumulator to the epilogue.
 //   warp 2      activation-scale loader: copies the tile's scale bytes (one
 //               row per token, up to 64 groups at a time) from global memory
-//               into a double-buffered compact buffer ahead of the producer,
-//               so the producer never waits on a global load.
+//               into a double-buffered compact buffer ahead of the producers.
 //   warps 3-10  epilogue: two warps per TMEM lane quadrant, each draining half
 //               of the tile's columns into registers, then releasing the
 //               accumulator to the MMA warp before rounding to BF16 and
 //               storing, so the next tile's MMAs overlap the stores.
-// Two orientations:
-//   normal  (many tokens): MMA M = 128 tokens, MMA N = 256 weight rows; the
-//           CTAs are persistent and walk the tiles with the weight tile
-//           fastest, so concurrent CTAs share A and W tiles through L2.
+//   warp 11     activation producer: per stage the TMA load of the activation
+//               tile and the stage's activation-scale atom, built from the
+//               compact buffer.  Weights and activations come from two warps
+//               because one thread completes only about one TMA copy every
+//               ~540 cycles.
+// Three forms:
+//   pair    (many tokens): a cluster of two CTAs issues the 2-SM MMA
+//           (tcgen05 cta_group::2): M = 256 tokens, 128 per CTA, N = 256
+//           weight rows, of which each CTA loads 128 while holding the scale
+//           atoms of all 256.  The CTA pairs are persistent and walk the
+//           units with the weight tile fastest, so concurrent pairs share A
+//           and W tiles through L2.
 //   swapped (few tokens):  MMA M = 128 weight rows, MMA N = 16..128 tokens, so
 //           the weight streams at full tile width with no padding of the token
 //           axis to 128.  The K range may be split over the CTAs of a
 //           thread-block cluster, whose fp32 partial tiles are summed in rank
 //           order through distributed shared memory (deterministic, no global
 //           workspace).
-// Fused activation form (swapped orientation, T <= 32): the activation is
-// read as BF16 straight from the attention output by TMA, and the epilogue
-// warps, idle during the mainloop, quantise each stage's tokens (inverse
-// RoPE on the last group, group-128 E8M0 scale, E4M3 codes) directly into
-// the 128-byte-swizzled operand tile and the scale atom the MMA reads.  One
-// launch then does the whole wo_a (or MXFP8 linear) step, with no round trip
-// of the codes through HBM.
+//   fused   (swapped, T <= 32): the activation is read as BF16 straight from
+//           the attention output by TMA, and the epilogue warps, idle during
+//           the mainloop, quantise each stage's tokens (inverse RoPE on the
+//           last group, group-128 E8M0 scale, E4M3 codes) directly into the
+//           128-byte-swizzled operand tile and the scale atom the MMA reads.
+//           One launch then does the whole wo_a (or MXFP8 linear) step, with
+//           no round trip of the codes through HBM.
 // Every wait is bounded in wall time; on expiry the kernel sets a watchdog
 // bit, stops issuing, drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -69,10 +75,13 @@ __device__ uint32_t g_watchdog;
 namespace {
 
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
+// Longest a pipeline wait (stage full / stage empty) may sleep before
+// re-checking: stages turn over every few hundred nanoseconds.
+constexpr uint32_t kPipeHintNs = 20;
 constexpr uint32_t kWdProducer = 1, kWdMma = 2, kWdEpilogue = 4, kWdDrain = 8, kWdLoader = 16;
-constexpr int kWarps = 11;
-constexpr int kThreads = kWarps * 32;
-constexpr int kEpiWarp0 = 3;
+constexpr int kEpiWarp0 = 3;   // epilogue warps 3-10
+constexpr int kEpiWarps = 8;
+constexpr int kActWarp = 11;   // activation producer (unfused forms)
 
 struct BmmArgs {
   const uint8_t* a_sf;  // [T][G][KG]
@@ -81,8 +90,9 @@ struct BmmArgs {
   int T, G, N, K, KG, NB;
   int x_tiles, y_tiles;  // tiles along the MMA-A rows (128) and MMA-B rows (BN)
   int splits, kg_per_split;
+  int x_span;            // rows of the MMA-A side per unit (256 for a CTA pair)
   int units;             // G * x_tiles * y_tiles * splits
-  int persistent;        // 1: each CTA walks units with stride gridDim.x
+  int persistent;        // 1: each CTA (pair) walks units with stride = CTAs (pairs) in the grid
   // Fused activation form only: positions, cos/sin cache, RoPE width.
   const int64_t* pos;
   const uint16_t* cos_tab;
@@ -92,14 +102,18 @@ struct BmmArgs {
   int32_t* err_flag;
 };
 
-template <bool SWAP, bool FUSED, int BN, int NSTAGE>
+// PAIR: the CTA-pair form (normal orientation only): MMA M = 256 tokens, 128
+// per CTA; MMA N = BN weight rows, of which each CTA loads half, while each
+// holds the scale atoms of all BN rows.
+template <bool SWAP, bool FUSED, int BN, int NSTAGE, bool PAIR = false>
 struct Cfg {
   static constexpr int BM = 128;
   static constexpr int BK = 128;
   static constexpr int Y_ATOMS = (BN + 127) / 128;
   static constexpr int ACT_ROWS = SWAP ? BN : BM;
   static constexpr int X_TILE = BM * BK;
-  static constexpr int Y_TILE = BN * BK;
+  static constexpr int Y_ROWS = PAIR ? BN / 2 : BN;  // MMA-B rows held by this CTA
+  static constexpr int Y_TILE = Y_ROWS * BK;
   static constexpr int SFX_BYTES = kSfAtomBytes;
   static constexpr int SFY_BYTES = Y_ATOMS * kSfAtomBytes;
   static constexpr int W_SF_BYTES = (SWAP ? 1 : Y_ATOMS) * kSfAtomBytes;
@@ -138,17 +152,21 @@ struct Cfg {
                                    : TMEM_USED <= 256 ? 256
                                                       : 512;
   static constexpr int HALF = BN / 2;        // columns drained by one epilogue warp
+  // The fused form quantises in the epilogue warps and needs no activation
+  // producer warp.
+  static constexpr int THREADS = (FUSED ? 11 : 12) * 32;
   // Instruction descriptor, kind::mxf8f6f4 with block scaling: E4M3 A and
   // B (format 0), both K-major, N >> 3 at bits 17-22, UE8M0 scale type at
   // bit 23, M >> 4 at bits 24-28, scale-factor ids 0.
   static constexpr uint32_t IDESC =
-      (1u << 23) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+      (1u << 23) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((PAIR ? 2 * BM : BM) >> 4) << 24);
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(!FUSED || (SWAP && BN <= 32), "fused activations: swapped form, <= 32 tokens");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
   static_assert(ACT_ROWS <= 128, "activation scale rows fit one loader pass");
   static_assert(HALF % 8 == 0, "epilogue drains 8-column chunks");
+  static_assert(!PAIR || (!SWAP && !FUSED && BN == 256), "pair form: normal orientation, N = 256");
 };
 
 __device__ __forceinline__ void watchdog(volatile int* abort_flag, uint32_t bit) {
@@ -184,18 +202,20 @@ __device__ __forceinline__ Unit decode_unit(const BmmArgs& p, int u) {
     r /= p.y_tiles;
   }
   w.g = r;
-  w.x0 = xt * 128;
+  w.x0 = xt * p.x_span;
   w.y0 = yt * BN;
   w.kg_begin = w.split * p.kg_per_split;
   w.nk = max(0, min(p.KG, w.kg_begin + p.kg_per_split) - w.kg_begin);
   return w;
 }
 
-template <bool SWAP, bool FUSED, int BN, int NSTAGE>
-__global__ void __launch_bounds__(kThreads, (Cfg<SWAP, FUSED, BN, NSTAGE>::CTAS_PER_SM))
+template <bool SWAP, bool FUSED, int BN, int NSTAGE, bool PAIR>
+__global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
+                                  (Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::CTAS_PER_SM))
     bmm_a8w8_kernel(const __grid_constant__ CUtensorMap tm_act,
-                    const __grid_constant__ CUtensorMap tm_w, const BmmArgs p) {
-  using C = Cfg<SWAP, FUSED, BN, NSTAGE>;
+                    const __grid_constant__ CUtensorMap tm_w,
+                    const __grid_constant__ CUtensorMap tm_wsf, const BmmArgs p) {
+  using C = Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -210,24 +230,33 @@ __global__ void __launch_bounds__(kThreads, (Cfg<SWAP, FUSED, BN, NSTAGE>::CTAS_
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_SLOT);
   uint8_t* csf = smem + C::OFF_CSF;
   __shared__ int abort_shared;
+  __shared__ int act_done_shared;  // stages the activation producer completed
   volatile int* abort_flag = &abort_shared;
+  volatile int* act_done = &act_done_shared;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int u_first = blockIdx.x;
-  const int u_step = p.persistent ? (int)gridDim.x : p.units;
+  // Pair form: CTAs 2i and 2i+1 share every unit; the even one issues the MMAs.
+  const uint32_t rank = PAIR ? ptx::cluster_rank() : 0u;
+  const int arow = PAIR ? 128 * (int)rank : 0;  // this CTA's first token row in the unit
+  const int u_first = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  // Pair form: every copy of both CTAs completes on the even CTA's barrier.
+  const uint32_t lead_full = PAIR ? ptx::map_shared_rank(ptx::smem_u32(full), 0) : 0u;
+  const int u_step = p.persistent ? (PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x) : p.units;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       // Unfused: the producer's weight arrival (with byte count) + its
       // scale-atom arrival.  Fused: one arrival per quantising warp; the
       // copies are tracked by `landed`.
-      ptx::mbar_init(&full[s], FUSED ? kWarps - kEpiWarp0 : 2);
+      // Pair form: the even CTA's barrier also takes the odd CTA's scale-atom
+      // arrival and counts the bytes of both CTAs' copies.
+      ptx::mbar_init(&full[s], FUSED ? kEpiWarps : (PAIR ? 3 : 2));
       ptx::mbar_init(&empty[s], 1);
       ptx::mbar_init(&landed[s], 1);
     }
     ptx::mbar_init(acc_full, 1);
-    ptx::mbar_init(acc_empty, kWarps - kEpiWarp0);
+    ptx::mbar_init(acc_empty, kEpiWarps * (PAIR ? 2 : 1));
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&sf_full[b], 32);
       ptx::mbar_init(&sf_empty[b], 1);
@@ -239,13 +268,20 @@ __global__ void __launch_bounds__(kThreads, (Cfg<SWAP, FUSED, BN, NSTAGE>::CTAS_
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tm_act);
     ptx::prefetch_tmap(&tm_w);
+    if (PAIR) ptx::prefetch_tmap(&tm_wsf);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(tmem_slot, C::TMEM_COLS);
-    ptx::tmem_relinquish();
+    if constexpr (PAIR) {
+      ptx::tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(tmem_slot, C::TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) ptx::cluster_sync();  // the peer's barriers exist before any remote arrive
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // The next kernel on the stream may be scheduled now: it only streams its
@@ -281,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<SWAP, FUSED, BN, NSTAGE>::CTAS_
         const uint32_t ph = (uint32_t)(it / NSTAGE) & 1u;
         const int kg = w.kg_begin + kk;
         if (it >= issued) {
-          if (*abort_flag || !ptx::mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs)) {
+          if (*abort_flag || !ptx::mbar_wait_hint(&empty[s], ph ^ 1u, kWaitLimitNs, kPipeHintNs)) {
             if (!*abort_flag) watchdog(abort_flag, kWdProducer);
             stop = true;
             break;
@@ -309,34 +345,94 @@ __global__ void __launch_bounds__(kThreads, (Cfg<SWAP, FUSED, BN, NSTAGE>::CTAS_
       }
     }
     } else {
-    // ------------------------------------------------------------ producer
-    // Stage bookkeeping (counters continue across units): stages < `it` are
-    // complete on the producer side; stages < `issued` have their weight
-    // copies in flight.  A stage's full barrier takes two arrivals (weights,
-    // with their byte count; then the activation-scale atom) plus the bytes
-    // of the activation tile, announced when that copy is issued.
-    int it = 0, issued = 0, ci = 0;
+    // ----------------------------------------------------- weight producer
+    // Stage bookkeeping (counters continue across units): stages < `issued`
+    // have their weight copies in flight.  A stage's full barrier takes the
+    // weight arrival (with its byte count) and the activation producer's
+    // arrival after its scale atom (the activation tile's bytes announced
+    // when that copy is issued); in the pair form the even CTA's barrier also
+    // takes the odd CTA's atom arrival and counts both CTAs' bytes.  Weights
+    // and activations are issued by two warps: one thread issues a TMA copy
+    // only every few hundred cycles, so a single issuing thread cannot keep
+    // the tensor cores fed.
+    int it = 0, issued = 0;
     bool stop = false;
     auto issue_weights = [&](const Unit& w, int s, int kg) {
       uint8_t* wt = smem + (SWAP ? C::OFF_X + s * C::X_TILE : C::OFF_Y + s * C::Y_TILE);
       uint8_t* wsf = smem + (SWAP ? C::OFF_SFX + s * C::SFX_BYTES : C::OFF_SFY + s * C::SFY_BYTES);
-      const int wrow0 = SWAP ? w.x0 : w.y0;
-      ptx::mbar_arrive_expect_tx(&full[s], (SWAP ? C::X_TILE : C::Y_TILE) + C::W_SF_BYTES);
-      ptx::tma_load_3d(wt, &tm_w, &full[s], kg * 128, wrow0, w.g);
-      ptx::bulk_load(wsf, p.w_sf + (((size_t)w.g * p.KG + kg) * p.NB + wrow0 / 128) * kSfAtomBytes,
-                     C::W_SF_BYTES, &full[s]);
+      const int wtile0 = SWAP ? w.x0 : w.y0;
+      const size_t atom0 = ((size_t)w.g * p.KG + kg) * p.NB + wtile0 / 128;
+      if constexpr (PAIR) {
+        // This CTA loads its half of the weight rows and the scale atoms of
+        // the whole tile; the even CTA announces the bytes of both.
+        const uint32_t bar = lead_full + 8u * (uint32_t)s;
+        if (rank == 0) ptx::mbar_arrive_expect_tx(&full[s], 2 * (C::Y_TILE + C::W_SF_BYTES));
+        ptx::tma_load_3d_pair(wt, &tm_w, bar, kg * 128, wtile0 + C::Y_ROWS * (int)rank, w.g);
+        ptx::tma_load_2d_pair(wsf, &tm_wsf, bar, 0, (int)(atom0 * (kSfAtomBytes / 256)));
+      } else {
+        ptx::mbar_arrive_expect_tx(&full[s], (SWAP ? C::X_TILE : C::Y_TILE) + C::W_SF_BYTES);
+        ptx::tma_load_3d(wt, &tm_w, &full[s], kg * 128, wtile0, w.g);
+        ptx::bulk_load(wsf, p.w_sf + atom0 * kSfAtomBytes, C::W_SF_BYTES, &full[s]);
+      }
     };
     // Weight tiles and scales do not depend on the preceding kernel: the
-    // first unit's first stages of weights are issued before waiting for it
-    // (programmatic dependent launch), so the weight stream starts while the
-    // quantiser is still finishing.
+    // first unit's first stages are issued before any wait, so the weight
+    // stream starts while that kernel is still finishing.
     if (u_first < p.units) {
       const Unit w = decode_unit<SWAP, BN>(p, u_first);
       issued = min(w.nk, NSTAGE);
       if (lane == 0)
         for (int kk = 0; kk < issued; ++kk) issue_weights(w, kk, w.kg_begin + kk);
     }
-    ptx::griddep_wait();
+    for (int u = u_first; u < p.units && !stop; u += u_step) {
+      const Unit w = decode_unit<SWAP, BN>(p, u);
+      for (int kk = 0; kk < w.nk; ++kk) {
+        const int s = it % NSTAGE;
+        const uint32_t ph = (uint32_t)(it / NSTAGE) & 1u;
+        if (it >= issued) {
+          if (*abort_flag || !ptx::mbar_wait_hint(&empty[s], ph ^ 1u, kWaitLimitNs, kPipeHintNs)) {
+            if (!*abort_flag) watchdog(abort_flag, kWdProducer);
+            stop = true;
+            break;
+          }
+          if (lane == 0) issue_weights(w, s, w.kg_begin + kk);
+          ++issued;
+        }
+        ++it;
+      }
+    }
+    // Meet the activation producer; after an abort, give every stage that
+    // has copies in flight the arrival it still lacks, so that its phase
+    // completes once the copies have landed, then drain.
+    ptx::named_sync(1, 64);
+    const int act_issued = *act_done;
+    if (lane == 0) {
+      for (int j = min(issued, act_issued); j < max(issued, act_issued); ++j) {
+        if (PAIR && rank != 0)
+          ptx::mbar_arrive_remote(lead_full + 8u * (uint32_t)(j % NSTAGE));
+        else
+          ptx::mbar_arrive(&full[j % NSTAGE]);
+      }
+    }
+    __syncwarp();
+    // Drain: every issued copy must have landed before exit (pair form: the
+    // even CTA's barriers count both CTAs' copies, and the odd CTA stays
+    // until the final cluster barrier).
+    const int last = max(issued, act_issued);
+    for (int j = max(0, last - NSTAGE); j < last && !(PAIR && rank != 0); ++j) {
+      if (!ptx::mbar_wait(&full[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1u, kWaitLimitNs)) {
+        watchdog(abort_flag, kWdDrain);
+        break;
+      }
+    }
+    }
+  } else if (warp == kActWarp) {
+    // ------------------------------------------------- activation producer
+    // (The fused form quantises in the epilogue warps; this warp idles.)
+    if constexpr (!FUSED) {
+    int it = 0, ci = 0;
+    bool stop = false;
+    ptx::griddep_wait();  // the activation codes come from the preceding kernel
     for (int u = u_first; u < p.units && !stop; u += u_step) {
       const Unit w = decode_unit<SWAP, BN>(p, u);
       for (int kk = 0; kk < w.nk; ++kk) {
@@ -344,14 +440,10 @@ __global__ void __launch_bounds__(kThreads, (Cfg<SWAP, FUSED, BN, NSTAGE>::CTAS_
         const int s = it % NSTAGE;
         const uint32_t ph = (uint32_t)(it / NSTAGE) & 1u;
         const int kg = w.kg_begin + kk;
-        if (it >= issued) {
-          if (*abort_flag || !ptx::mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs)) {
-            if (!*abort_flag) watchdog(abort_flag, kWdProducer);
-            stop = true;
-            break;
-          }
-          if (lane == 0) issue_weights(w, s, kg);
-          ++issued;
+        if (*abort_flag || !ptx::mbar_wait_hint(&empty[s], ph ^ 1u, kWaitLimitNs, kPipeHintNs)) {
+          if (!*abort_flag) watchdog(abort_flag, kWdProducer);
+          stop = true;
+          break;
         }
         if ((kk % C::SF_CHUNK) == 0 &&
             !ptx::mbar_wait(&sf_full[b], (uint32_t)(ci >> 1) & 1u, kWaitLimitNs)) {
@@ -361,8 +453,14 @@ __global__ void __launch_bounds__(kThreads, (Cfg<SWAP, FUSED, BN, NSTAGE>::CTAS_
         }
         if (lane == 0) {
           uint8_t* at = smem + (SWAP ? C::OFF_Y + s * C::Y_TILE : C::OFF_X + s * C::X_TILE);
-          ptx::mbar_expect_tx(&full[s], SWAP ? C::Y_TILE : C::X_TILE);
-          ptx::tma_load_3d(at, &tm_act, &full[s], kg * 128, w.g, SWAP ? w.y0 : w.x0);
+          if constexpr (PAIR) {
+            if (rank == 0) ptx::mbar_expect_tx(&full[s], 2 * C::X_TILE);
+            ptx::tma_load_3d_pair(at, &tm_act, lead_full + 8u * (uint32_t)s, kg * 128, w.g,
+                                  w.x0 + arow);
+          } else {
+            ptx::mbar_expect_tx(&full[s], SWAP ? C::Y_TILE : C::X_TILE);
+            ptx::tma_load_3d(at, &tm_act, &full[s], kg * 128, w.g, SWAP ? w.y0 : w.x0);
+          }
         }
         // Activation-scale atom: lane i writes the 16-byte line of rows
         // i, i+32, i+64, i+96 (one word each, the byte replicated four times).
@@ -376,7 +474,12 @@ __global__ void __launch_bounds__(kThreads, (Cfg<SWAP, FUSED, BN, NSTAGE>::CTAS_
         *reinterpret_cast<uint4*>(asf + lane * 16) = line;
         ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&full[s]);
+        if (lane == 0) {
+          if (PAIR && rank != 0)
+            ptx::mbar_arrive_remote(lead_full + 8u * (uint32_t)s);
+          else
+            ptx::mbar_arrive(&full[s]);
+        }
         ++it;
         if ((kk % C::SF_CHUNK) == C::SF_CHUNK - 1 || kk == w.nk - 1) {
           if (lane == 0) ptx::mbar_arrive(&sf_empty[b]);
@@ -384,19 +487,11 @@ __global__ void __launch_bounds__(kThreads, (Cfg<SWAP, FUSED, BN, NSTAGE>::CTAS_
         }
       }
     }
-    // After an abort, stages with weights in flight but no second arrival get
-    // it now, so that their phase completes once the copies have landed.
-    if (lane == 0)
-      for (int j = it; j < issued; ++j) ptx::mbar_arrive(&full[j % NSTAGE]);
-    __syncwarp();
-    // Drain: every issued copy must have landed before exit.
-    for (int j = max(0, issued - NSTAGE); j < issued; ++j) {
-      if (!ptx::mbar_wait(&full[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1u, kWaitLimitNs)) {
-        watchdog(abort_flag, kWdDrain);
-        break;
-      }
+    if (lane == 0) *act_done = it;
+    ptx::named_sync(1, 64);
     }
-    }
+  } else if (warp == 1 && PAIR && rank != 0) {
+    // Pair form, odd CTA: the even CTA issues every MMA and scale copy.
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     int it = 0, ti = 0;
@@ -411,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<SWAP, FUSED, BN, NSTAGE>::CTAS_
       for (int kk = 0; kk < w.nk; ++kk) {
         const int s = it % NSTAGE;
         const uint32_t ph = (uint32_t)(it / NSTAGE) & 1u;
-        if (*abort_flag || !ptx::mbar_wait(&full[s], ph, kWaitLimitNs)) {
+        if (*abort_flag || !ptx::mbar_wait_hint(&full[s], ph, kWaitLimitNs, kPipeHintNs)) {
           if (!*abort_flag) watchdog(abort_flag, kWdMma);
           stop = true;
           break;
@@ -424,30 +519,54 @@ __global__ void __launch_bounds__(kThreads, (Cfg<SWAP, FUSED, BN, NSTAGE>::CTAS_
           const uint32_t ys = ptx::smem_u32(smem + C::OFF_Y + s * C::Y_TILE);
           const uint32_t sfx = ptx::smem_u32(smem + C::OFF_SFX + s * C::SFX_BYTES);
           const uint32_t sfy = ptx::smem_u32(smem + C::OFF_SFY + s * C::SFY_BYTES);
-          ptx::tmem_cp_32x128b_x4(sfx_col, ptx::smem_desc(sfx, 128, 128, ptx::kSwizzleNone));
-#pragma unroll
-          for (int a = 0; a < C::Y_ATOMS; ++a)
-            ptx::tmem_cp_32x128b_x4(
-                sfy_col + 4 * a,
-                ptx::smem_desc(sfy + a * kSfAtomBytes, 128, 128, ptx::kSwizzleNone));
           const uint64_t adesc = ptx::smem_desc(xs, 16, 1024, ptx::kSwizzle128B);
           const uint64_t bdesc = ptx::smem_desc(ys, 16, 1024, ptx::kSwizzle128B);
+          if constexpr (PAIR) {
+            ptx::tmem_cp_32x128b_x4_pair(sfx_col, ptx::smem_desc(sfx, 128, 128, ptx::kSwizzleNone));
 #pragma unroll
-          for (int k = 0; k < 4; ++k)  // 4 x (K = 32 bytes) inside the 128-byte swizzle row
-            ptx::mma_mxf8(tmem, adesc + 2 * k, bdesc + 2 * k, C::IDESC, sfx_col, sfy_col,
-                          (kk > 0 || k > 0) ? 1u : 0u);
-          ptx::tc_commit(&empty[s]);
+            for (int a = 0; a < C::Y_ATOMS; ++a)
+              ptx::tmem_cp_32x128b_x4_pair(
+                  sfy_col + 4 * a,
+                  ptx::smem_desc(sfy + a * kSfAtomBytes, 128, 128, ptx::kSwizzleNone));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              ptx::mma_mxf8_pair(tmem, adesc + 2 * k, bdesc + 2 * k, C::IDESC, sfx_col, sfy_col,
+                                 (kk > 0 || k > 0) ? 1u : 0u);
+            ptx::tc_commit_pair_mc(&empty[s], 3);  // frees the stage in both CTAs
+          } else {
+            ptx::tmem_cp_32x128b_x4(sfx_col, ptx::smem_desc(sfx, 128, 128, ptx::kSwizzleNone));
+#pragma unroll
+            for (int a = 0; a < C::Y_ATOMS; ++a)
+              ptx::tmem_cp_32x128b_x4(
+                  sfy_col + 4 * a,
+                  ptx::smem_desc(sfy + a * kSfAtomBytes, 128, 128, ptx::kSwizzleNone));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)  // 4 x (K = 32 bytes) inside the 128-byte swizzle row
+              ptx::mma_mxf8(tmem, adesc + 2 * k, bdesc + 2 * k, C::IDESC, sfx_col, sfy_col,
+                            (kk > 0 || k > 0) ? 1u : 0u);
+            ptx::tc_commit(&empty[s]);
+          }
         }
         __syncwarp();
         ++it;
       }
       if (stop) break;
-      if (lane == 0) ptx::tc_commit(acc_full);
+      if (lane == 0) {
+        if constexpr (PAIR)
+          ptx::tc_commit_pair_mc(acc_full, 3);
+        else
+          ptx::tc_commit(acc_full);
+      }
       __syncwarp();
       ++ti;
     }
     // Every MMA and scale copy this warp issued must finish before TMEM is freed.
-    if (lane == 0) ptx::tc_commit(mma_done);
+    if (lane == 0) {
+      if constexpr (PAIR)
+        ptx::tc_commit_pair_mc(mma_done, 1);
+      else
+        ptx::tc_commit(mma_done);
+    }
     __syncwarp();
     if (!ptx::mbar_wait(mma_done, 0, kWaitLimitNs)) watchdog(abort_flag, kWdDrain);
   } else if (warp == 2) {
@@ -458,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<SWAP, FUSED, BN, NSTAGE>::CTAS_
     bool stop = false;
     for (int u = u_first; u < p.units && !stop; u += u_step) {
       const Unit w = decode_unit<SWAP, BN>(p, u);
-      const int row0 = SWAP ? w.y0 : w.x0;
+      const int row0 = SWAP ? w.y0 : w.x0 + arow;
       if (u == u_first) ptx::griddep_wait();  // the scales come from the preceding kernel
       for (int c0 = 0; c0 < w.nk; c0 += C::SF_CHUNK) {
         const int b = ci & 1;
@@ -514,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<SWAP, FUSED, BN, NSTAGE>::CTAS_
     if constexpr (FUSED) {
       // Scale-atom rows past the token tile (BN < 128) never change: 127.
       const int te = threadIdx.x - kEpiWarp0 * 32;
-      for (int i = te; i < NSTAGE * (128 - BN); i += (kWarps - kEpiWarp0) * 32) {
+      for (int i = te; i < NSTAGE * (128 - BN); i += kEpiWarps * 32) {
         const int s = i / (128 - BN);
         const int rr = BN + i % (128 - BN);
         *reinterpret_cast<uint32_t*>(smem + C::OFF_SFY + s * C::SFY_BYTES + (rr & 31) * 16 +
@@ -636,7 +755,12 @@ __global__ void __launch_bounds__(kThreads, (Cfg<SWAP, FUSED, BN, NSTAGE>::CTAS_
       ptx::tmem_ld_wait();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(acc_empty);  // the accumulator may be overwritten now
+      if (lane == 0) {  // the accumulator may be overwritten now
+        if constexpr (PAIR)
+          ptx::mbar_arrive_remote(ptx::map_shared_rank(ptx::smem_u32(acc_empty), 0));
+        else
+          ptx::mbar_arrive(acc_empty);
+      }
       ++ti;
       if (w.nk == 0) {
 #pragma unroll
@@ -644,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<SWAP, FUSED, BN, NSTAGE>::CTAS_
       }
       const int c0 = h * C::HALF;
       if (!SWAP) {
-        const int t = w.x0 + r;
+        const int t = w.x0 + arow + r;
         if (t < p.T) {
           __nv_bfloat16* orow = p.out + ((size_t)t * p.G + w.g) * p.N + w.y0 + c0;
 #pragma unroll
@@ -700,7 +824,7 @@ __global__ void __launch_bounds__(kThreads, (Cfg<SWAP, FUSED, BN, NSTAGE>::CTAS_
       // BF16 stores of a warp are contiguous along n.
       const float* red = reinterpret_cast<const float*>(smem + C::OFF_RED);
       const int tv4 = (tv + 3) >> 2;
-      for (int e = threadIdx.x; e < nrows * tv4; e += kThreads) {
+      for (int e = threadIdx.x; e < nrows * tv4; e += C::THREADS) {
         const int tl = (e / nrows) * 4;
         const int rr = e % nrows;
         float4 acc = *reinterpret_cast<const float4*>(red + rr * C::PART_PITCH + tl);
@@ -723,9 +847,13 @@ __global__ void __launch_bounds__(kThreads, (Cfg<SWAP, FUSED, BN, NSTAGE>::CTAS_
       }
     }
   }
+  if constexpr (PAIR) ptx::cluster_sync();  // no CTA leaves while its peer may still use it
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+    if constexpr (PAIR)
+      ptx::tmem_dealloc_pair(tmem, C::TMEM_COLS);
+    else
+      ptx::tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
@@ -775,21 +903,40 @@ bool encode_3d(CUtensorMap* m, const void* base, bool bf16, uint64_t d0, uint64_
   return r == CUDA_SUCCESS;
 }
 
-template <bool SWAP, bool FUSED, int BN, int NSTAGE>
+// 2-D uint8 map over the prepared weight scales, 256-byte rows (two per
+// 512-byte atom), boxes of `rows` rows: the pair form's scale-atom copies.
+bool encode_scale_rows(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {256, rows};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {256, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool SWAP, bool FUSED, int BN, int NSTAGE, bool PAIR = false>
 cudaError_t launch_cfg(const void* a, const uint8_t* w, BmmArgs args, int num_sms,
                        cudaStream_t s, const char** why) {
-  using C = Cfg<SWAP, FUSED, BN, NSTAGE>;
+  using C = Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>;
   const uint64_t K = args.K, G = args.G, T = args.T, N = args.N;
   CUtensorMap tm_act, tm_w;
   const uint32_t act_box = SWAP ? BN : C::BM;
-  const uint32_t w_box = SWAP ? C::BM : BN;
+  const uint32_t w_box = SWAP ? C::BM : C::Y_ROWS;
   const uint64_t esz = FUSED ? 2 : 1;  // fused form: x is BF16
+  CUtensorMap tm_wsf = {};
+  const uint64_t atoms = G * (uint64_t)args.KG * (uint64_t)args.NB;
   if (!encode_3d(&tm_act, a, FUSED, K, G, T, K * esz, G * K * esz, 128, 1, act_box) ||
-      !encode_3d(&tm_w, w, false, K, N, G, K, N * K, 128, w_box, 1)) {
+      !encode_3d(&tm_w, w, false, K, N, G, K, N * K, 128, w_box, 1) ||
+      (PAIR && !encode_scale_rows(&tm_wsf, args.w_sf, atoms * (kSfAtomBytes / 256),
+                                  (uint32_t)(C::W_SF_BYTES / 256)))) {
     *why = "cuTensorMapEncodeTiled failed (driver entry point missing or arguments rejected)";
     return cudaErrorInvalidValue;
   }
-  auto kern = bmm_a8w8_kernel<SWAP, FUSED, BN, NSTAGE>;
+  auto kern = bmm_a8w8_kernel<SWAP, FUSED, BN, NSTAGE, PAIR>;
   // The shared-memory opt-in is set once per device (a host-side call that
   // must not run inside stream capture, so the first call on a device should
   // happen before any capture).
@@ -819,11 +966,8 @@ cudaError_t launch_cfg(const void* a, const uint8_t* w, BmmArgs args, int num_sm
   }
   args.units = args.G * args.x_tiles * args.y_tiles * args.splits;
   args.persistent = args.splits == 1 ? 1 : 0;
-  const int slots = num_sms * C::CTAS_PER_SM;
-  const int grid = args.persistent ? (args.units < slots ? args.units : slots) : args.units;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = s;
   // Programmatic dependent launch: the grid may start while the preceding
@@ -834,14 +978,37 @@ cudaError_t launch_cfg(const void* a, const uint8_t* w, BmmArgs args, int num_sm
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (args.splits > 1) {
+  const int cluster = PAIR ? 2 : args.splits;
+  if (cluster > 1) {
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = (unsigned)args.splits;
+    attr[1].val.clusterDim.x = (unsigned)cluster;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  return cudaLaunchKernelEx(&cfg, kern, tm_act, tm_w, args);
+  int grid = args.units;
+  if (PAIR) {
+    // One persistent CTA pair per co-resident cluster slot (the SM pairs the
+    // GPCs can form), each pair walking the units.
+    static std::atomic<int> pair_slots[64];
+    int slots = pair_slots[dev & 63].load(std::memory_order_acquire);
+    if (slots == 0) {
+      cfg.gridDim = dim3(2u * (unsigned)(num_sms / 2), 1, 1);
+      e = cudaOccupancyMaxActiveClusters(&slots, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (slots <= 0) {
+        *why = "no CTA pair fits on this device";
+        return cudaErrorInvalidConfiguration;
+      }
+      pair_slots[dev & 63].store(slots, std::memory_order_release);
+    }
+    grid = 2 * (args.units < slots ? args.units : slots);
+  } else if (args.persistent) {
+    const int slots = num_sms * C::CTAS_PER_SM;
+    grid = args.units < slots ? args.units : slots;
+  }
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, tm_act, tm_w, tm_wsf, args);
 }
 
 }  // namespace
@@ -861,6 +1028,7 @@ cudaError_t launch_bmm_a8w8(const uint8_t* a, const uint8_t* a_sf, const uint8_t
   args.NB = (int)sf_row_blocks(N);
   if (T <= 128) {
     // Few tokens: weight rows on the MMA M axis, tokens on N.
+    args.x_span = 128;
     args.x_tiles = (int)ceil_div(N, 128);
     args.y_tiles = 1;
     if (T <= 16) return launch_cfg<true, false, 16, 5>(a, w, args, num_sms, s, why);
@@ -868,11 +1036,13 @@ cudaError_t launch_bmm_a8w8(const uint8_t* a, const uint8_t* a_sf, const uint8_t
     if (T <= 64) return launch_cfg<true, false, 64, 6>(a, w, args, num_sms, s, why);
     return launch_cfg<true, false, 128, 4>(a, w, args, num_sms, s, why);
   }
-  args.x_tiles = (int)ceil_div(T, 128);
+  // Many tokens: CTA pairs, 256 tokens x 256 weight rows per unit.
+  args.x_span = 256;
+  args.x_tiles = (int)ceil_div(T, 256);
   args.y_tiles = (int)ceil_div(N, 256);
   args.splits = 1;
   args.kg_per_split = args.KG;
-  return launch_cfg<false, false, 256, 4>(a, w, args, num_sms, s, why);
+  return launch_cfg<false, false, 256, 6, true>(a, w, args, num_sms, s, why);
 }
 
 cudaError_t launch_wo_a_fused(const void* x, const int64_t* pos, const void* cos, const void* sin,
@@ -895,6 +1065,7 @@ cudaError_t launch_wo_a_fused(const void* x, const int64_t* pos, const void* cos
   args.max_pos = max_pos;
   args.R = R;
   args.err_flag = err_flag;
+  args.x_span = 128;
   args.x_tiles = (int)ceil_div(N, 128);
   args.y_tiles = 1;
   if (T <= 16) return launch_cfg<true, true, 16, 4>(x, w, args, num_sms, s, why);
