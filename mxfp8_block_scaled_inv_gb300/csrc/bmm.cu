@@ -134,7 +134,12 @@ struct Cfg {
   static constexpr int RED_ROWS = 136;
   static constexpr int RED_BYTES = SWAP ? RED_ROWS * PART_PITCH * 4 : 0;
   static constexpr int OFF_RED = OFF_CSF + 2 * CSF_BYTES;
-  static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
+  // Pair form: per epilogue warp, two 32 x 32 BF16 staging tiles for the
+  // TMA stores of the output.
+  static constexpr int OUT_TILE = 32 * 32 * 2;
+  static constexpr int OUT_BYTES = PAIR ? 8 * 2 * OUT_TILE : 0;
+  static constexpr int OFF_OUT = OFF_RED + RED_BYTES;
+  static constexpr int OFF_BAR = OFF_OUT + OUT_BYTES;
   // full[NSTAGE], empty[NSTAGE], landed[NSTAGE], acc_full, acc_empty,
   // sf_full[2], sf_empty[2], mma_done
   static constexpr int N_BARS = 3 * NSTAGE + 7;
@@ -214,7 +219,8 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
                                   (Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::CTAS_PER_SM))
     bmm_a8w8_kernel(const __grid_constant__ CUtensorMap tm_act,
                     const __grid_constant__ CUtensorMap tm_w,
-                    const __grid_constant__ CUtensorMap tm_wsf, const BmmArgs p) {
+                    const __grid_constant__ CUtensorMap tm_wsf,
+                    const __grid_constant__ CUtensorMap tm_out, const BmmArgs p) {
   using C = Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -767,7 +773,34 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
         for (int j = 0; j < C::HALF; ++j) v[j] = 0u;  // an empty K slice contributes zero
       }
       const int c0 = h * C::HALF;
-      if (!SWAP) {
+      if constexpr (PAIR) {
+        // Rows of a lane are 16 KB apart in the output, so each warp stages
+        // 32 rows x 32 columns in shared memory and one lane stores the box
+        // with TMA (full lines, no per-lane scattered stores; rows past T
+        // and columns past N are clipped by the copy).
+        uint8_t* stg = smem + C::OFF_OUT + (warp - kEpiWarp0) * 2 * C::OUT_TILE;
+#pragma unroll
+        for (int c = 0; c < C::HALF / 32; ++c) {
+          uint8_t* buf = stg + (c & 1) * C::OUT_TILE;
+          if (lane == 0) ptx::bulk_wait_read<1>();  // the store two chunks back has read it
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 o;
+            o.x = pack_bf16x2(v[c * 32 + j * 8 + 0], v[c * 32 + j * 8 + 1]);
+            o.y = pack_bf16x2(v[c * 32 + j * 8 + 2], v[c * 32 + j * 8 + 3]);
+            o.z = pack_bf16x2(v[c * 32 + j * 8 + 4], v[c * 32 + j * 8 + 5]);
+            o.w = pack_bf16x2(v[c * 32 + j * 8 + 6], v[c * 32 + j * 8 + 7]);
+            *reinterpret_cast<uint4*>(buf + lane * 64 + j * 16) = o;
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(&tm_out, buf, w.y0 + c0 + c * 32, w.g, w.x0 + arow + q * 32);
+            ptx::bulk_commit_group();
+          }
+        }
+      } else if (!SWAP) {
         const int t = w.x0 + arow + r;
         if (t < p.T) {
           __nv_bfloat16* orow = p.out + ((size_t)t * p.G + w.g) * p.N + w.y0 + c0;
@@ -807,6 +840,11 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
     }
   }
 
+  if constexpr (PAIR) {
+    // The output stores must be complete (and their shared-memory sources
+    // read) before the CTA retires.
+    if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps && lane == 0) ptx::bulk_wait_all();
+  }
   __syncthreads();
   if (SWAP && p.splits > 1) {
     // Deterministic split-K reduction over the cluster (one unit per CTA).
@@ -927,12 +965,14 @@ cudaError_t launch_cfg(const void* a, const uint8_t* w, BmmArgs args, int num_sm
   const uint32_t act_box = SWAP ? BN : C::BM;
   const uint32_t w_box = SWAP ? C::BM : C::Y_ROWS;
   const uint64_t esz = FUSED ? 2 : 1;  // fused form: x is BF16
-  CUtensorMap tm_wsf = {};
+  CUtensorMap tm_wsf = {}, tm_out = {};
   const uint64_t atoms = G * (uint64_t)args.KG * (uint64_t)args.NB;
   if (!encode_3d(&tm_act, a, FUSED, K, G, T, K * esz, G * K * esz, 128, 1, act_box) ||
       !encode_3d(&tm_w, w, false, K, N, G, K, N * K, 128, w_box, 1) ||
       (PAIR && !encode_scale_rows(&tm_wsf, args.w_sf, atoms * (kSfAtomBytes / 256),
-                                  (uint32_t)(C::W_SF_BYTES / 256)))) {
+                                  (uint32_t)(C::W_SF_BYTES / 256))) ||
+      // Output [T][G][N] BF16, 32 x 32 boxes of one group (pair-form epilogue).
+      (PAIR && !encode_3d(&tm_out, args.out, true, N, G, T, N * 2, G * N * 2, 32, 1, 32))) {
     *why = "cuTensorMapEncodeTiled failed (driver entry point missing or arguments rejected)";
     return cudaErrorInvalidValue;
   }
@@ -1008,7 +1048,7 @@ cudaError_t launch_cfg(const void* a, const uint8_t* w, BmmArgs args, int num_sm
     grid = args.units < slots ? args.units : slots;
   }
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, tm_act, tm_w, tm_wsf, args);
+  return cudaLaunchKernelEx(&cfg, kern, tm_act, tm_w, tm_wsf, tm_out, args);
 }
 
 }  // namespace
@@ -1042,7 +1082,7 @@ cudaError_t launch_bmm_a8w8(const uint8_t* a, const uint8_t* a_sf, const uint8_t
   args.y_tiles = (int)ceil_div(N, 256);
   args.splits = 1;
   args.kg_per_split = args.KG;
-  return launch_cfg<false, false, 256, 6, true>(a, w, args, num_sms, s, why);
+  return launch_cfg<false, false, 256, 5, true>(a, w, args, num_sms, s, why);
 }
 
 cudaError_t launch_wo_a_fused(const void* x, const int64_t* pos, const void* cos, const void* sin,
