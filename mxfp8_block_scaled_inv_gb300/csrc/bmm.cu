@@ -82,6 +82,7 @@ constexpr uint32_t kWdProducer = 1, kWdMma = 2, kWdEpilogue = 4, kWdDrain = 8, k
 constexpr int kEpiWarp0 = 3;   // epilogue warps 3-10
 constexpr int kEpiWarps = 8;
 constexpr int kActWarp = 11;   // activation producer (unfused forms)
+constexpr int kGateWarp = 12;  // pair form: waits on the MMA warp's barriers
 
 struct BmmArgs {
   const uint8_t* a_sf;  // [T][G][KG]
@@ -159,7 +160,10 @@ struct Cfg {
   static constexpr int HALF = BN / 2;        // columns drained by one epilogue warp
   // The fused form quantises in the epilogue warps and needs no activation
   // producer warp.
-  static constexpr int THREADS = (FUSED ? 11 : 12) * 32;
+  // The pair form adds a gate warp that does the MMA warp's barrier waits:
+  // the tensor pipe's instruction queue is shallow, so any wait in the
+  // issuing warp between stages leaves the pipe idle.
+  static constexpr int THREADS = (FUSED ? 11 : (PAIR ? 13 : 12)) * 32;
   // Instruction descriptor, kind::mxf8f6f4 with block scaling: E4M3 A and
   // B (format 0), both K-major, N >> 3 at bits 17-22, UE8M0 scale type at
   // bit 23, M >> 4 at bits 24-28, scale-factor ids 0.
@@ -237,8 +241,10 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
   uint8_t* csf = smem + C::OFF_CSF;
   __shared__ int abort_shared;
   __shared__ int act_done_shared;  // stages the activation producer completed
+  __shared__ int gate_go_shared[2];  // pair form: stage handed over (1) or stop (0)
   volatile int* abort_flag = &abort_shared;
   volatile int* act_done = &act_done_shared;
+  volatile int* gate_go = gate_go_shared;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -504,15 +510,25 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
     bool stop = false;
     for (int u = u_first; u < p.units && !stop; u += u_step) {
       const Unit w = decode_unit<SWAP, BN>(p, u);
-      if (*abort_flag || !ptx::mbar_wait(acc_empty, (uint32_t)(ti & 1) ^ 1u, kWaitLimitNs)) {
-        if (!*abort_flag) watchdog(abort_flag, kWdMma);
-        break;
+      if constexpr (!PAIR) {
+        if (*abort_flag || !ptx::mbar_wait(acc_empty, (uint32_t)(ti & 1) ^ 1u, kWaitLimitNs)) {
+          if (!*abort_flag) watchdog(abort_flag, kWdMma);
+          break;
+        }
+        ptx::tc_fence_after();
       }
-      ptx::tc_fence_after();
       for (int kk = 0; kk < w.nk; ++kk) {
         const int s = it % NSTAGE;
         const uint32_t ph = (uint32_t)(it / NSTAGE) & 1u;
-        if (*abort_flag || !ptx::mbar_wait_hint(&full[s], ph, kWaitLimitNs, kPipeHintNs)) {
+        if constexpr (PAIR) {
+          // The gate warp has seen this stage land (and, before a unit's
+          // first stage, the accumulator drained); meet it.
+          ptx::named_sync(2, 64);
+          if (!gate_go[it & 1]) {
+            stop = true;
+            break;
+          }
+        } else if (*abort_flag || !ptx::mbar_wait_hint(&full[s], ph, kWaitLimitNs, kPipeHintNs)) {
           if (!*abort_flag) watchdog(abort_flag, kWdMma);
           stop = true;
           break;
@@ -626,6 +642,35 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
         ++ci;
       }
     }
+    }
+  } else if (warp == kGateWarp) {
+    // ---------------------------------------------------- gate (pair form)
+    // Waits, for the even CTA's MMA warp, on the accumulator at each unit's
+    // start and on each stage's full barrier, then meets the MMA warp at a
+    // named barrier.  Both warps pass that barrier exactly once per stage
+    // (or once more with "stop" after a failed bounded wait, then both
+    // leave), and the go flag alternates between two slots so that it is
+    // never rewritten before the MMA warp has read it.
+    if constexpr (PAIR) {
+      if (rank == 0) {
+        int it = 0, ti = 0;
+        bool ok = true;
+        for (int u = u_first; u < p.units && ok; u += u_step) {
+          const Unit w = decode_unit<SWAP, BN>(p, u);
+          ok = !*abort_flag && ptx::mbar_wait(acc_empty, (uint32_t)(ti & 1) ^ 1u, kWaitLimitNs);
+          for (int kk = 0; kk < w.nk; ++kk) {
+            const int s = it % NSTAGE;
+            const uint32_t ph = (uint32_t)(it / NSTAGE) & 1u;
+            ok = ok && !*abort_flag && ptx::mbar_wait_hint(&full[s], ph, kWaitLimitNs, kPipeHintNs);
+            if (lane == 0) gate_go[it & 1] = ok ? 1 : 0;
+            ptx::named_sync(2, 64);
+            if (!ok) break;
+            ++it;
+          }
+          ++ti;
+        }
+        if (!ok && !*abort_flag) watchdog(abort_flag, kWdMma);
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -750,6 +795,49 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
         break;
       }
       ptx::tc_fence_after();
+      if constexpr (PAIR) {
+        // Drain 32 columns at a time and keep them as packed BF16 pairs (RNE,
+        // as in the other forms), so that the 13-warp CTA fits its register
+        // budget; the accumulator is released as soon as it is read.
+        uint32_t pk[C::HALF / 2];
+#pragma unroll
+        for (int c = 0; c < C::HALF / 32; ++c) {
+          uint32_t t32[32];
+          ptx::tmem_ld_32x32b_x32(trow + c * 32, t32);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pk[c * 16 + j] = pack_bf16x2(t32[2 * j], t32[2 * j + 1]);
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0)  // the accumulator may be overwritten now
+          ptx::mbar_arrive_remote(ptx::map_shared_rank(ptx::smem_u32(acc_empty), 0));
+        ++ti;
+        // Rows of a lane are 16 KB apart in the output, so each warp stages
+        // 32 rows x 32 columns in shared memory and one lane stores the box
+        // with TMA (full lines, no per-lane scattered stores; rows past T
+        // and columns past N are clipped by the copy).
+        const int c0 = h * C::HALF;
+        uint8_t* stg = smem + C::OFF_OUT + (warp - kEpiWarp0) * 2 * C::OUT_TILE;
+#pragma unroll
+        for (int c = 0; c < C::HALF / 32; ++c) {
+          uint8_t* buf = stg + (c & 1) * C::OUT_TILE;
+          if (lane == 0) ptx::bulk_wait_read<1>();  // the store two chunks back has read it
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(buf + lane * 64 + j * 16) =
+                make_uint4(pk[c * 16 + j * 4 + 0], pk[c * 16 + j * 4 + 1], pk[c * 16 + j * 4 + 2],
+                           pk[c * 16 + j * 4 + 3]);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(&tm_out, buf, w.y0 + c0 + c * 32, w.g, w.x0 + arow + q * 32);
+            ptx::bulk_commit_group();
+          }
+        }
+        continue;
+      }
       uint32_t v[C::HALF];
       if constexpr (C::HALF % 32 == 0) {
 #pragma unroll
@@ -761,46 +849,14 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
       ptx::tmem_ld_wait();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) {  // the accumulator may be overwritten now
-        if constexpr (PAIR)
-          ptx::mbar_arrive_remote(ptx::map_shared_rank(ptx::smem_u32(acc_empty), 0));
-        else
-          ptx::mbar_arrive(acc_empty);
-      }
+      if (lane == 0) ptx::mbar_arrive(acc_empty);  // the accumulator may be overwritten now
       ++ti;
       if (w.nk == 0) {
 #pragma unroll
         for (int j = 0; j < C::HALF; ++j) v[j] = 0u;  // an empty K slice contributes zero
       }
       const int c0 = h * C::HALF;
-      if constexpr (PAIR) {
-        // Rows of a lane are 16 KB apart in the output, so each warp stages
-        // 32 rows x 32 columns in shared memory and one lane stores the box
-        // with TMA (full lines, no per-lane scattered stores; rows past T
-        // and columns past N are clipped by the copy).
-        uint8_t* stg = smem + C::OFF_OUT + (warp - kEpiWarp0) * 2 * C::OUT_TILE;
-#pragma unroll
-        for (int c = 0; c < C::HALF / 32; ++c) {
-          uint8_t* buf = stg + (c & 1) * C::OUT_TILE;
-          if (lane == 0) ptx::bulk_wait_read<1>();  // the store two chunks back has read it
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint4 o;
-            o.x = pack_bf16x2(v[c * 32 + j * 8 + 0], v[c * 32 + j * 8 + 1]);
-            o.y = pack_bf16x2(v[c * 32 + j * 8 + 2], v[c * 32 + j * 8 + 3]);
-            o.z = pack_bf16x2(v[c * 32 + j * 8 + 4], v[c * 32 + j * 8 + 5]);
-            o.w = pack_bf16x2(v[c * 32 + j * 8 + 6], v[c * 32 + j * 8 + 7]);
-            *reinterpret_cast<uint4*>(buf + lane * 64 + j * 16) = o;
-          }
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::tma_store_3d(&tm_out, buf, w.y0 + c0 + c * 32, w.g, w.x0 + arow + q * 32);
-            ptx::bulk_commit_group();
-          }
-        }
-      } else if (!SWAP) {
+      if (!SWAP) {
         const int t = w.x0 + arow + r;
         if (t < p.T) {
           __nv_bfloat16* orow = p.out + ((size_t)t * p.G + w.g) * p.N + w.y0 + c0;
