@@ -120,7 +120,7 @@ struct Cfg {
   static constexpr int W_SF_BYTES = (SWAP ? 1 : Y_ATOMS) * kSfAtomBytes;
   // Compact activation-scale buffer: groups per chunk (a few-token CTA
   // holds only a short K slice, so its chunks are smaller).
-  static constexpr int SF_CHUNK = SWAP ? 16 : 64;
+  static constexpr int SF_CHUNK = (SWAP || PAIR) ? 16 : 64;
   static constexpr int CSF_BYTES = FUSED ? 0 : SF_CHUNK * 128;  // [group][128 rows]
   static constexpr int STG_BYTES = FUSED ? BN * 256 : 0;         // BF16 staging [BN][128]
   static constexpr int OFF_X = 0;
@@ -135,10 +135,10 @@ struct Cfg {
   static constexpr int RED_ROWS = 136;
   static constexpr int RED_BYTES = SWAP ? RED_ROWS * PART_PITCH * 4 : 0;
   static constexpr int OFF_RED = OFF_CSF + 2 * CSF_BYTES;
-  // Pair form: per epilogue warp, two 32 x 32 BF16 staging tiles for the
+  // Pair form: per epilogue warp, one 32 x 32 BF16 staging tile for the
   // TMA stores of the output.
   static constexpr int OUT_TILE = 32 * 32 * 2;
-  static constexpr int OUT_BYTES = PAIR ? 8 * 2 * OUT_TILE : 0;
+  static constexpr int OUT_BYTES = PAIR ? 8 * OUT_TILE : 0;
   static constexpr int OFF_OUT = OFF_RED + RED_BYTES;
   static constexpr int OFF_BAR = OFF_OUT + OUT_BYTES;
   // full[NSTAGE], empty[NSTAGE], landed[NSTAGE], acc_full, acc_empty,
@@ -375,12 +375,17 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
       const int wtile0 = SWAP ? w.x0 : w.y0;
       const size_t atom0 = ((size_t)w.g * p.KG + kg) * p.NB + wtile0 / 128;
       if constexpr (PAIR) {
-        // This CTA loads its half of the weight rows and the scale atoms of
-        // the whole tile; the even CTA announces the bytes of both.
+        // This CTA loads its half of the weight rows (lane 0) and the scale
+        // atoms of the whole tile (lane 1: each thread issues only about one
+        // TMA copy every few hundred cycles); the even CTA announces the
+        // bytes of both CTAs.
         const uint32_t bar = lead_full + 8u * (uint32_t)s;
-        if (rank == 0) ptx::mbar_arrive_expect_tx(&full[s], 2 * (C::Y_TILE + C::W_SF_BYTES));
-        ptx::tma_load_3d_pair(wt, &tm_w, bar, kg * 128, wtile0 + C::Y_ROWS * (int)rank, w.g);
-        ptx::tma_load_2d_pair(wsf, &tm_wsf, bar, 0, (int)(atom0 * (kSfAtomBytes / 256)));
+        if (lane == 0) {
+          if (rank == 0) ptx::mbar_arrive_expect_tx(&full[s], 2 * (C::Y_TILE + C::W_SF_BYTES));
+          ptx::tma_load_3d_pair(wt, &tm_w, bar, kg * 128, wtile0 + C::Y_ROWS * (int)rank, w.g);
+        } else {
+          ptx::tma_load_2d_pair(wsf, &tm_wsf, bar, 0, (int)(atom0 * (kSfAtomBytes / 256)));
+        }
       } else {
         ptx::mbar_arrive_expect_tx(&full[s], (SWAP ? C::X_TILE : C::Y_TILE) + C::W_SF_BYTES);
         ptx::tma_load_3d(wt, &tm_w, &full[s], kg * 128, wtile0, w.g);
@@ -393,7 +398,7 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
     if (u_first < p.units) {
       const Unit w = decode_unit<SWAP, BN>(p, u_first);
       issued = min(w.nk, NSTAGE);
-      if (lane == 0)
+      if (lane < (PAIR ? 2 : 1))
         for (int kk = 0; kk < issued; ++kk) issue_weights(w, kk, w.kg_begin + kk);
     }
     for (int u = u_first; u < p.units && !stop; u += u_step) {
@@ -407,7 +412,7 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
             stop = true;
             break;
           }
-          if (lane == 0) issue_weights(w, s, w.kg_begin + kk);
+          if (lane < (PAIR ? 2 : 1)) issue_weights(w, s, w.kg_begin + kk);
           ++issued;
         }
         ++it;
@@ -657,7 +662,8 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
         bool ok = true;
         for (int u = u_first; u < p.units && ok; u += u_step) {
           const Unit w = decode_unit<SWAP, BN>(p, u);
-          ok = !*abort_flag && ptx::mbar_wait(acc_empty, (uint32_t)(ti & 1) ^ 1u, kWaitLimitNs);
+          ok = !*abort_flag &&
+               ptx::mbar_wait_hint(acc_empty, (uint32_t)(ti & 1) ^ 1u, kWaitLimitNs, kPipeHintNs);
           for (int kk = 0; kk < w.nk; ++kk) {
             const int s = it % NSTAGE;
             const uint32_t ph = (uint32_t)(it / NSTAGE) & 1u;
@@ -789,7 +795,8 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
         }
         if (qstop) break;
       }
-      const bool waited = !*abort_flag && ptx::mbar_wait(acc_full, (uint32_t)(ti & 1), kWaitLimitNs);
+      const bool waited =
+          !*abort_flag && ptx::mbar_wait_hint(acc_full, (uint32_t)(ti & 1), kWaitLimitNs, kPipeHintNs);
       if (!__all_sync(0xffffffffu, waited)) {
         if (!*abort_flag) watchdog(abort_flag, kWdEpilogue);
         break;
@@ -818,11 +825,10 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
         // with TMA (full lines, no per-lane scattered stores; rows past T
         // and columns past N are clipped by the copy).
         const int c0 = h * C::HALF;
-        uint8_t* stg = smem + C::OFF_OUT + (warp - kEpiWarp0) * 2 * C::OUT_TILE;
+        uint8_t* buf = smem + C::OFF_OUT + (warp - kEpiWarp0) * C::OUT_TILE;
 #pragma unroll
         for (int c = 0; c < C::HALF / 32; ++c) {
-          uint8_t* buf = stg + (c & 1) * C::OUT_TILE;
-          if (lane == 0) ptx::bulk_wait_read<1>();  // the store two chunks back has read it
+          if (lane == 0) ptx::bulk_wait_read<0>();  // the previous chunk's store has read it
           __syncwarp();
 #pragma unroll
           for (int j = 0; j < 4; ++j)
@@ -1138,7 +1144,7 @@ cudaError_t launch_bmm_a8w8(const uint8_t* a, const uint8_t* a_sf, const uint8_t
   args.y_tiles = (int)ceil_div(N, 256);
   args.splits = 1;
   args.kg_per_split = args.KG;
-  return launch_cfg<false, false, 256, 5, true>(a, w, args, num_sms, s, why);
+  return launch_cfg<false, false, 256, 6, true>(a, w, args, num_sms, s, why);
 }
 
 cudaError_t launch_wo_a_fused(const void* x, const int64_t* pos, const void* cos, const void* sin,
