@@ -140,3 +140,35 @@ def test_empty_tokens_is_noop(mxq):
     wd, swd = to_dev(w, sw)
     out = mxq.mxq_bmm_a8w8(a, sa, wd, mxq.mxq_prepare_weight_scales(swd, 256))
     assert out.shape == (0, 2, 128)
+
+
+@pytest.mark.parametrize("T,G,N,K", [(257, 1, 16, 256), (257, 2, 48, 384), (384, 1, 272, 2304),
+                                     (1000, 3, 1040, 640)])
+def test_pair_form_edges(mxq, T, G, N, K):
+    """Many-token (CTA-pair) form at its edges: the odd CTA's 128 tokens partly
+    or wholly past T (T = 257, 384), weight tiles mostly past N (N = 16, 48,
+    272, 1040), one group, unaligned K; TMA clips the output stores."""
+    a, sa, w, sw = random_operands(T, G, N, K, seed=1200 + T + N)
+    check_gemm(run_bmm(mxq, a, sa, w, sw), *O.bmm_a8w8_ref(a, sa, w, sw), f"pair T={T} N={N}")
+
+
+def test_pair_form_deterministic(mxq):
+    a, sa, w, sw = random_operands(600, 4, 512, 1024, seed=1300)
+    o1 = run_bmm(mxq, a, sa, w, sw)
+    o2 = run_bmm(mxq, a, sa, w, sw)
+    assert torch.equal(o1, o2)
+
+
+def test_pair_form_leaves_padding_untouched(mxq):
+    """Rows past T and columns past N are not written by the clipped stores:
+    out is a view into a larger buffer whose surroundings stay intact."""
+    T, G, N, K = 300, 2, 48, 256
+    a, sa, w, sw = random_operands(T, G, N, K, seed=1400)
+    ad, sad, wd, swd = to_dev(a, sa, w, sw)
+    wsf = mxq.mxq_prepare_weight_scales(swd, K)
+    big = torch.full((T + 5, G, N), -7.0, dtype=torch.bfloat16, device="cuda")
+    out = big[:T]
+    mxq.mxq_bmm_a8w8(ad, sad, wd, wsf, out=out)
+    torch.cuda.synchronize()
+    assert bool((big[T:] == -7.0).all())
+    check_gemm(out, *O.bmm_a8w8_ref(a, sa, w, sw), "pair padding")
