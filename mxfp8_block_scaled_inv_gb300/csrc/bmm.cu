@@ -118,8 +118,9 @@ struct Cfg {
   static constexpr int SFX_BYTES = kSfAtomBytes;
   static constexpr int SFY_BYTES = Y_ATOMS * kSfAtomBytes;
   static constexpr int W_SF_BYTES = (SWAP ? 1 : Y_ATOMS) * kSfAtomBytes;
-  // Compact activation-scale buffer: groups per chunk (a few-token CTA
-  // holds only a short K slice, so its chunks are smaller).
+  // Compact activation-scale buffer: groups per chunk (a few-token CTA holds
+  // only a short K slice; the pair form spends the shared memory on a sixth
+  // pipeline stage instead).
   static constexpr int SF_CHUNK = (SWAP || PAIR) ? 16 : 64;
   static constexpr int CSF_BYTES = FUSED ? 0 : SF_CHUNK * 128;  // [group][128 rows]
   static constexpr int STG_BYTES = FUSED ? BN * 256 : 0;         // BF16 staging [BN][128]
@@ -258,9 +259,9 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
-      // Unfused: the producer's weight arrival (with byte count) + its
-      // scale-atom arrival.  Fused: one arrival per quantising warp; the
-      // copies are tracked by `landed`.
+      // Unfused: the weight producer's arrival (with the weight bytes) and
+      // the activation producer's arrival after its scale atom.  Fused: one
+      // arrival per quantising warp; the copies are tracked by `landed`.
       // Pair form: the even CTA's barrier also takes the odd CTA's scale-atom
       // arrival and counts the bytes of both CTAs' copies.
       ptx::mbar_init(&full[s], FUSED ? kEpiWarps : (PAIR ? 3 : 2));
