@@ -16,7 +16,7 @@ peak), secondary workloads (decode latency per layer, the unaligned-K
 linear, the dequantiser, the 100K-token stream), the CPU oracle timed on a
 bounded sample, and the SM clocks sampled during the timed region.
 
---impl reference times the CPU oracle (the reference arm of this build)
+--impl reference times the CPU oracle (the reference arm)
 on bounded samples of the same workload.
 """
 

@@ -23,7 +23,7 @@ What it computes, and where each step comes from:
   2^(scale byte - 127), rounded once to BF16; the unaligned shapes are
   K = 576 and 288.
 
-Readings taken where the pages are silent (each one is listed in the design doc):
+Readings taken where the pages are silent:
 
 * Scale rule: e = ceil(log2(amax / 448)), i.e. the smallest integer e with
   amax <= 448 * 2^e, evaluated exactly (no floating log2 or division);
@@ -38,7 +38,7 @@ Readings taken where the pages are silent (each one is listed in the design doc):
   quantisation.
 * A partial last group (K % 128 != 0) takes its amax over the elements that
   exist.
-* GEMM reference: exact products summed in fp64; GPU results are judged by
+* GEMM reference: exact products summed in fp64; GPU results are checked by
   |y - y_ref| <= 1 bf16 ulp(y_ref) + 1e-5 * sum_k |a_k w_k|.
 
 Parity is pinned by tests/test_oracle_*.py (hand-worked examples, library
