@@ -389,6 +389,32 @@ def cpu_baseline(budget_s=12.0):
                       f"one thread"}
 
 
+# ---------------------------------------------------------- multi-rank glue
+def rank_env():
+    """(world size, rank, local rank) as torchrun sets them; one process = 1."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value, device=None):
+    """The largest `value` over all ranks: a job's step time is its slowest
+    rank's.  Identity outside a process group of more than one rank."""
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    on = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=on)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, units_per_rank, ms_step):
+    """Whole-job rate: every rank processes its own units (weak scaling, no
+    exchange) and the job takes as long as its slowest rank."""
+    return world * units_per_rank / (ms_step * 1e-3)
+
+
 def prefill_config(world):
     """The headline workload, as both arms report it."""
     return {"workload": "wo_a prefill chunk: x [8192,8,4096] bf16 (1% x50 outliers), "
@@ -498,9 +524,7 @@ def main():
     ap.add_argument("--k", type=int, default=576, help="K of the linear workload")
     args = ap.parse_args()
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local_rank = rank_env()
     if args.impl == "reference":
         return run_reference(args, rank)
 
@@ -578,11 +602,8 @@ def main():
     t_quant = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
     t_gemm = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
     ms_step = ms_total / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = world * T_PREFILL / (ms_step * 1e-3)
+    ms_step = max_over_ranks(ms_step, device)
+    value = job_throughput(world, T_PREFILL, ms_step)
 
     # End to end through the public API: pinned host x -> device, wo_a, output
     # -> host, every step.  The steps are pipelined on three streams (copy
@@ -646,11 +667,8 @@ def main():
         b.record(s_out)
     torch.cuda.synchronize()
     e2e_ms = a.elapsed_time(b) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * T_PREFILL / (e2e_ms * 1e-3)
+    e2e_ms = max_over_ranks(e2e_ms, device)
+    e2e_value = job_throughput(world, T_PREFILL, e2e_ms)
     h2d = x_host.numel() * 2 + pos_host.numel() * 8
     d2h = out_host.numel() * 2
     del x_host, out_host
