@@ -75,8 +75,9 @@ __device__ uint32_t g_watchdog;
 namespace {
 
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
-// Longest a pipeline wait (stage full / stage empty) may sleep before
-// re-checking: stages turn over every few hundred nanoseconds.
+// Longest a pipeline wait may sleep before re-checking: stages turn over
+// every few hundred nanoseconds, and a plain try_wait measured up to ~1.6 us
+// late in waking after its phase completed.
 constexpr uint32_t kPipeHintNs = 20;
 constexpr uint32_t kWdProducer = 1, kWdMma = 2, kWdEpilogue = 4, kWdDrain = 8, kWdLoader = 16;
 constexpr int kEpiWarp0 = 3;   // epilogue warps 3-10
@@ -464,7 +465,7 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
           break;
         }
         if ((kk % C::SF_CHUNK) == 0 &&
-            !ptx::mbar_wait(&sf_full[b], (uint32_t)(ci >> 1) & 1u, kWaitLimitNs)) {
+            !ptx::mbar_wait_hint(&sf_full[b], (uint32_t)(ci >> 1) & 1u, kWaitLimitNs, kPipeHintNs)) {
           watchdog(abort_flag, kWdProducer);
           stop = true;
           break;
@@ -517,7 +518,8 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
     for (int u = u_first; u < p.units && !stop; u += u_step) {
       const Unit w = decode_unit<SWAP, BN>(p, u);
       if constexpr (!PAIR) {
-        if (*abort_flag || !ptx::mbar_wait(acc_empty, (uint32_t)(ti & 1) ^ 1u, kWaitLimitNs)) {
+        if (*abort_flag ||
+            !ptx::mbar_wait_hint(acc_empty, (uint32_t)(ti & 1) ^ 1u, kWaitLimitNs, kPipeHintNs)) {
           if (!*abort_flag) watchdog(abort_flag, kWdMma);
           break;
         }
@@ -610,7 +612,8 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
       for (int c0 = 0; c0 < w.nk; c0 += C::SF_CHUNK) {
         const int b = ci & 1;
         if (*abort_flag ||
-            !ptx::mbar_wait(&sf_empty[b], ((uint32_t)(ci >> 1) & 1u) ^ 1u, kWaitLimitNs)) {
+            !ptx::mbar_wait_hint(&sf_empty[b], ((uint32_t)(ci >> 1) & 1u) ^ 1u, kWaitLimitNs,
+                                 kPipeHintNs)) {
           if (!*abort_flag) watchdog(abort_flag, kWdLoader);
           stop = true;
           break;
@@ -740,7 +743,8 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
         for (int kk = 0; kk < w.nk; ++kk) {
           const int s = itq % NSTAGE;
           const uint32_t ph = (uint32_t)(itq / NSTAGE) & 1u;
-          const bool ok_wait = !*abort_flag && ptx::mbar_wait(&landed[s], ph, kWaitLimitNs);
+          const bool ok_wait =
+              !*abort_flag && ptx::mbar_wait_hint(&landed[s], ph, kWaitLimitNs, kPipeHintNs);
           if (!__all_sync(0xffffffffu, ok_wait)) {
             if (!*abort_flag) watchdog(abort_flag, kWdEpilogue);
             qstop = true;
