@@ -42,6 +42,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __global__ void __launch_bounds__(kThreads) dequant_bf16_kernel(
     const uint4* __restrict__ w, const uint8_t* __restrict__ sc, uint4* __restrict__ out,
     uint32_t n_chunks, uint32_t chunks_per_row, int KG) {
+  // Launched with programmatic dependent launch: wait for the preceding
+  // kernel's writes before reading, and let the next kernel start launching.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (uint32_t c = blockIdx.x * kThreads + threadIdx.x; c < n_chunks; c += gridDim.x * kThreads) {
     const uint32_t row = c / chunks_per_row;
     const uint32_t kc = c - row * chunks_per_row;
@@ -112,10 +116,17 @@ cudaError_t launch_dequant_bf16(const uint8_t* w, const uint8_t* sc, void* out, 
   const uint32_t chunks_per_row = (uint32_t)(K / 16);
   const uint32_t n_chunks = (uint32_t)((int64_t)B * N * chunks_per_row);
   const int KG = (int)ceil_div(K, kGroup);
-  dequant_bf16_kernel<<<grid_for(n_chunks, kThreads, num_sms), kThreads, 0, s>>>(
-      reinterpret_cast<const uint4*>(w), sc, reinterpret_cast<uint4*>(out), n_chunks,
-      chunks_per_row, KG);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid_for(n_chunks, kThreads, num_sms), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, dequant_bf16_kernel, reinterpret_cast<const uint4*>(w), sc,
+                            reinterpret_cast<uint4*>(out), n_chunks, chunks_per_row, KG);
 }
 
 cudaError_t launch_prepare_weight_scales(const uint8_t* w_e8m0, int B, int N, int K, uint8_t* out,
