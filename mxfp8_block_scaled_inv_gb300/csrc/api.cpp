@@ -246,6 +246,7 @@ size_t mxq_wo_a_workspace_bytes(int64_t T, int32_t G, int32_t D, int32_t N) {
   (void)N;
   if (T < 0 || G < 1 || D < 1) return 0;
   if (T <= mxq::kFusedMaxTokens) return 0;
+  if (T >= mxq::kPairMinTokens) return mxq::woa_prefill_layout(T, G, D).total;
   return round256((size_t)T * G * D) + round256((size_t)T * G * kgroups(D));
 }
 
@@ -290,6 +291,18 @@ int mxq_wo_a(const void* x_bf16, const int64_t* pos, const void* cos_bf16, const
   if (!ws || ws_bytes < need)
     return fail(MXQ_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, ws_bytes);
   if (!aligned16(ws)) return fail(MXQ_ERR_ALIGN, "workspace must be 16-byte aligned");
+  if (T >= mxq::kPairMinTokens) {
+    if (T * G * kgroups(D) >= (int64_t)1 << 31)
+      return fail(MXQ_ERR_UNSUPPORTED, "T*G*ceil(D/128) must be < 2^31");
+    int sms = 0;
+    if (int st = device_check(&sms)) return st;
+    const char* why = nullptr;
+    cudaError_t e = mxq::launch_wo_a_prefill(x_bf16, pos, cos_bf16, sin_bf16, cs_ld, max_pos, R,
+                                             w_e4m3, w_sf_prepared, out_bf16, T, G, N, D, err_flag,
+                                             ws, sms, static_cast<cudaStream_t>(stream), &why);
+    if (e != cudaSuccess && why) return fail(MXQ_ERR_CUDA, "wo_a: %s", why);
+    return cuda_status(e, "wo_a (quantising pair form) launch");
+  }
   uint8_t* codes = static_cast<uint8_t*>(ws);
   uint8_t* scales = codes + round256((size_t)T * G * D);
   if (int st = mxq_inv_rope_group_quant(x_bf16, T, G, D, R, pos, cos_bf16, sin_bf16, cs_ld, max_pos,

@@ -53,6 +53,21 @@
 //           128-byte-swizzled operand tile and the scale atom the MMA reads.
 //           One launch then does the whole wo_a (or MXFP8 linear) step, with
 //           no round trip of the codes through HBM.
+//   pair + quantise (many tokens, wo_a): the pair form, reading the BF16
+//           activation.  Four more warps of each CTA (warp 2 and warps 13-15)
+//           quantise the CTA's own 128 token rows (inverse RoPE on the last
+//           group, group scale, E4M3 codes) into a workspace, ahead of the
+//           MMAs and independently of them: the codes go to global memory in
+//           the [T][G][K] layout and the scale bytes as ready-made scale atoms,
+//           and a per-(128 rows, K group) counter in global memory is raised
+//           once the writes are visible.  The units of one 256-token block
+//           are taken by consecutive pairs, and the pair with weight tile yt
+//           quantises the K groups kg = yt (mod weight tiles) of the block, so
+//           the quantisation is spread over every SM and done once.  The
+//           activation producer polls the counters and TMA-loads the codes
+//           and atoms as soon as they are published.  The quantising warps
+//           never wait on anything, so the counters always complete (every
+//           CTA of the persistent grid is resident).
 // Every wait is bounded in wall time; on expiry the kernel sets a watchdog
 // bit, stops issuing, drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -61,6 +76,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <utility>
 #include <mutex>
 
 #include "mxq.h"
@@ -84,6 +100,25 @@ constexpr int kEpiWarp0 = 3;   // epilogue warps 3-10
 constexpr int kEpiWarps = 8;
 constexpr int kActWarp = 11;   // activation producer (unfused forms)
 constexpr int kGateWarp = 12;  // pair form: waits on the MMA warp's barriers
+// Quantising pair form: warp 2 loads the BF16 activation slices (16 rows x
+// 128 values, 4 KB) with TMA, and warps 13-15 quantise them, slice n going to
+// warp n % kQWorkers; each of those warps owns a ring of kQRing slots that it
+// consumes in order.  A job (128 rows of one K group) is kQSlices slices and
+// its counter reaches kQSlices.
+constexpr int kQProducerWarp = 2;
+constexpr int kQWarpHi = 13;
+constexpr int kQWorkers = 3;
+constexpr int kQSlices = 8;
+constexpr int kQRows = 128 / kQSlices;
+constexpr int kQSliceBytes = kQRows * 128 * 2;
+constexpr int kQRing = 3;
+constexpr int kQSlots = kQWorkers * kQRing;
+constexpr int kQMetaBytes = 32 + 8 * kQRows;
+// Longest sleep between two polls of a not-yet-published counter.
+constexpr uint32_t kFlagPollNs = 128;
+// Publications are batched: the gpu-scope fence waits for every store the
+// warp still has in flight.
+constexpr int kQPublish = 8;
 
 struct BmmArgs {
   const uint8_t* a_sf;  // [T][G][KG]
@@ -102,12 +137,19 @@ struct BmmArgs {
   int64_t cs_ld, max_pos;
   int R;
   int32_t* err_flag;
+  // Quantising pair form only: BF16 input and the workspace it fills.
+  const uint16_t* xq;  // [T][G][K] BF16
+  uint8_t* qcodes;     // [T][G][K] E4M3 codes (read back as the A operand)
+  uint8_t* qatoms;     // [G][MB][KG][512] activation scale atoms
+  uint32_t* qflags;    // [G][MB][KG] job counters, zero before the launch
+  int MB;              // 128-token blocks per group (2 * x_tiles)
 };
 
 // PAIR: the CTA-pair form (normal orientation only): MMA M = 256 tokens, 128
 // per CTA; MMA N = BN weight rows, of which each CTA loads half, while each
-// holds the scale atoms of all BN rows.
-template <bool SWAP, bool FUSED, int BN, int NSTAGE, bool PAIR = false>
+// holds the scale atoms of all BN rows.  QUANT (pair form only): the kernel
+// quantises the BF16 activation itself.
+template <bool SWAP, bool FUSED, int BN, int NSTAGE, bool PAIR = false, bool QUANT = false>
 struct Cfg {
   static constexpr int BM = 128;
   static constexpr int BK = 128;
@@ -123,7 +165,7 @@ struct Cfg {
   // only a short K slice; the pair form spends the shared memory on a sixth
   // pipeline stage instead).
   static constexpr int SF_CHUNK = (SWAP || PAIR) ? 16 : 64;
-  static constexpr int CSF_BYTES = FUSED ? 0 : SF_CHUNK * 128;  // [group][128 rows]
+  static constexpr int CSF_BYTES = (FUSED || QUANT) ? 0 : SF_CHUNK * 128;  // [group][128 rows]
   static constexpr int STG_BYTES = FUSED ? BN * 256 : 0;         // BF16 staging [BN][128]
   static constexpr int OFF_X = 0;
   static constexpr int OFF_Y = OFF_X + NSTAGE * X_TILE;
@@ -142,10 +184,15 @@ struct Cfg {
   static constexpr int OUT_TILE = 32 * 32 * 2;
   static constexpr int OUT_BYTES = PAIR ? 8 * OUT_TILE : 0;
   static constexpr int OFF_OUT = OFF_RED + RED_BYTES;
-  static constexpr int OFF_BAR = OFF_OUT + OUT_BYTES;
+  // Quantising form: the BF16 activation slices.
+  static constexpr int QX_BYTES = QUANT ? kQSlots * kQSliceBytes : 0;
+  static constexpr int OFF_QX = OFF_OUT + OUT_BYTES;
+  static constexpr int QM_BYTES = QUANT ? kQSlots * kQMetaBytes : 0;  // slice descriptions
+  static constexpr int OFF_QM = OFF_QX + QX_BYTES;
+  static constexpr int OFF_BAR = OFF_QM + QM_BYTES;
   // full[NSTAGE], empty[NSTAGE], landed[NSTAGE], acc_full, acc_empty,
-  // sf_full[2], sf_empty[2], mma_done
-  static constexpr int N_BARS = 3 * NSTAGE + 7;
+  // sf_full[2], sf_empty[2], mma_done, then qfull[kQSlots], qempty[kQSlots]
+  static constexpr int N_BARS = 3 * NSTAGE + 7 + (QUANT ? 2 * kQSlots : 0);
   static constexpr int OFF_SLOT = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_SLOT + 16 + 1024;
   // Two CTAs share an SM when their shared memory allows it (the small-token
@@ -165,7 +212,9 @@ struct Cfg {
   // The pair form adds a gate warp that does the MMA warp's barrier waits:
   // the tensor pipe's instruction queue is shallow, so any wait in the
   // issuing warp between stages leaves the pipe idle.
-  static constexpr int THREADS = (FUSED ? 11 : (PAIR ? 13 : 12)) * 32;
+  // The quantising pair form adds the quantising warps (warp 2, the scale
+  // loader otherwise, loads their slices).
+  static constexpr int THREADS = (FUSED ? 11 : (PAIR ? (QUANT ? kQWarpHi + kQWorkers : 13) : 12)) * 32;
   // Instruction descriptor, kind::mxf8f6f4 with block scaling: E4M3 A and
   // B (format 0), both K-major, N >> 3 at bits 17-22, UE8M0 scale type at
   // bit 23, M >> 4 at bits 24-28, scale-factor ids 0.
@@ -178,6 +227,7 @@ struct Cfg {
   static_assert(ACT_ROWS <= 128, "activation scale rows fit one loader pass");
   static_assert(HALF % 8 == 0, "epilogue drains 8-column chunks");
   static_assert(!PAIR || (!SWAP && !FUSED && BN == 256), "pair form: normal orientation, N = 256");
+  static_assert(!QUANT || PAIR, "in-kernel quantisation: pair form only");
 };
 
 __device__ __forceinline__ void watchdog(volatile int* abort_flag, uint32_t bit) {
@@ -220,14 +270,379 @@ __device__ __forceinline__ Unit decode_unit(const BmmArgs& p, int u) {
   return w;
 }
 
-template <bool SWAP, bool FUSED, int BN, int NSTAGE, bool PAIR>
-__global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
-                                  (Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::CTAS_PER_SM))
+// ------------------------------------------- in-kernel activation quantisation
+// A job = one K group kg of one 128-token block of one group g, done by the
+// CTA that owns the block as kQSlices slices of kQRows rows.  The quantising
+// producer (warp 2) TMA-loads each slice's BF16 values into a slot of the
+// ring of the warp that will quantise it; that warp quantises the slice into
+// global memory and raises the job's counter by one, so a finished job's
+// counter reads kQSlices.
+struct QJob {
+  int u, jj;  // unit and job index within the unit
+  int g, kg;  // group and K group
+  int t0;     // first token of the 128-token block
+  int f;      // counter / atom index: (g * MB + block) * KG + kg
+};
+
+// Job jj of unit u for CTA `rank` of the pair: of the y_tiles pairs that
+// share a 256-token block, the one holding weight tile yt quantises K groups
+// r, r + y_tiles, ... with r = (yt + block) mod y_tiles, so that the rotated
+// last group (the slowest) moves from pair to pair with the block.
+__device__ __forceinline__ bool qjob_make(const BmmArgs& p, int u, int jj, int rank, QJob& j) {
+  const Unit w = decode_unit<false, 256>(p, u);
+  const int kg = (w.y0 / 256 + w.x0 / 256) % p.y_tiles + jj * p.y_tiles;
+  if (kg >= p.KG) return false;
+  const int blk = w.x0 / 128 + rank;
+  j.u = u;
+  j.jj = jj;
+  j.g = w.g;
+  j.kg = kg;
+  j.t0 = blk * 128;
+  j.f = (w.g * p.MB + blk) * p.KG + kg;
+  return true;
+}
+
+// Advances j to the next job of this CTA (units u, u + u_step, ...).
+__device__ __forceinline__ bool qjob_next(const BmmArgs& p, int u_step, int rank, QJob& j) {
+  if (j.kg + p.y_tiles < p.KG) {  // the same unit's next K group
+    ++j.jj;
+    j.kg += p.y_tiles;
+    j.f += p.y_tiles;
+    return true;
+  }
+  for (int u = j.u + u_step; u < p.units; u += u_step)
+    if (qjob_make(p, u, 0, rank, j)) return true;
+  return false;
+}
+
+__device__ __forceinline__ bool qjob_first(const BmmArgs& p, int u_first, int u_step, int rank,
+                                           QJob& j) {
+  for (int u = u_first; u < p.units; u += u_step)
+    if (qjob_make(p, u, 0, rank, j)) return true;
+  return false;
+}
+
+// Slot of the k-th slice of quantising warp w (its own ring, used in order).
+__device__ __forceinline__ int qslot(int w, int k) { return w * kQRing + k % kQRing; }
+
+// Description of the slice in a slot, written by the producer beside the
+// copy (the quantising warps then need no job walk and no position loads).
+struct QMeta {
+  int g, kg, t0, f;           // job fields (t0 = the block's first token)
+  int s;                      // slice within the job
+  uint32_t bad;               // bit r: row r has an invalid position
+  int pad[2];
+  int64_t pos[kQRows];        // positions of the rows (0 past T, or without RoPE)
+};
+static_assert(sizeof(QMeta) == kQMetaBytes, "slice description size");
+
+// Producer: slices in order, two per round (lanes 0 and 1 each issue one
+// copy: a thread issues only about one TMA copy every few hundred cycles;
+// lanes 16 h + r describe row r of the round's slice h).  Slice n is the
+// (n / kQWorkers)-th slice of warp n % kQWorkers; its slot is refilled once
+// that warp has released the slice kQRing before it.  The positions of the
+// next round are loaded while this one waits.
+__device__ __forceinline__ void quant_producer(const BmmArgs& p, const CUtensorMap* tm_x,
+                                               uint8_t* qx, QMeta* qm, uint64_t* qfull,
+                                               uint64_t* qempty, int u_first, int u_step, int rank,
+                                               int lane, volatile int* abort_flag) {
+  QJob j;
+  if (!qjob_first(p, u_first, u_step, rank, j)) return;
+  ptx::griddep_wait();  // x and the positions come from preceding work
+  const int half = lane >> 4;
+  const int row = lane & 15;
+  auto pos_of = [&](const QJob& jj, int sl) -> int64_t {
+    const int t = jj.t0 + kQRows * sl + row;
+    return (p.R > 0 && t < p.T) ? __ldg(p.pos + t) : 0;
+  };
+  int s = 0;
+  int64_t pcur = pos_of(j, half);
+  int n = 0;
+  while (true) {
+    QJob j2 = j;
+    int s2 = s + 2;
+    bool more = true;
+    if (s2 == kQSlices) {
+      s2 = 0;
+      more = qjob_next(p, u_step, rank, j2);
+    }
+    const int64_t pnext = more ? pos_of(j2, s2 + half) : 0;
+    bool ok = !*abort_flag;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int m = n + h;
+      const int k = m / kQWorkers;
+      if (ok && k >= kQRing)
+        ok = ptx::mbar_wait_hint(&qempty[qslot(m % kQWorkers, k)],
+                                 (uint32_t)((k / kQRing) - 1) & 1u, kWaitLimitNs, kPipeHintNs);
+    }
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0 && !*abort_flag) watchdog(abort_flag, kWdLoader);
+      break;
+    }
+    {
+      const int t = j.t0 + kQRows * (s + half) + row;
+      const bool bad = p.R > 0 && t < p.T && (pcur < 0 || pcur >= p.max_pos);
+      const uint32_t bm = __ballot_sync(0xffffffffu, bad);
+      const int m = n + half;
+      QMeta* md = qm + qslot(m % kQWorkers, m / kQWorkers);
+      md->pos[row] = pcur;
+      if (row == 0) {
+        md->g = j.g;
+        md->kg = j.kg;
+        md->t0 = j.t0;
+        md->f = j.f;
+        md->s = s + half;
+        md->bad = (bm >> (16 * half)) & 0xFFFFu;
+      }
+    }
+    __syncwarp();  // the descriptions are written before the copies' arrivals
+    if (lane < 2) {
+      const int m = n + lane;
+      const int slot = qslot(m % kQWorkers, m / kQWorkers);
+      ptx::mbar_arrive_expect_tx(&qfull[slot], kQSliceBytes);
+      ptx::tma_load_3d(qx + slot * kQSliceBytes, tm_x, &qfull[slot], j.kg * 128, j.g,
+                       j.t0 + kQRows * (s + lane));
+    }
+    __syncwarp();
+    n += 2;
+    pcur = pnext;
+    if (!more) break;
+    j = j2;
+    s = s2;
+  }
+  // Every issued copy lands before the CTA may retire (the quantising warps
+  // consume them all unless a wait ran out): the last issued slice of every
+  // slot, whose phase is the slot's latest.
+  for (int m = max(0, n - kQSlots); m < n; ++m) {
+    const int k = m / kQWorkers;
+    if (!ptx::mbar_wait(&qfull[qslot(m % kQWorkers, k)], (uint32_t)(k / kQRing) & 1u,
+                        kWaitLimitNs)) {
+      if (lane == 0) watchdog(abort_flag, kWdDrain);
+      break;
+    }
+  }
+}
+
+// Quantises a rotated slice (the row's last group when R > 0; one in KG
+// jobs): steps of two rows, a half-warp per row and 8 values per lane, with
+// the arithmetic of the standalone quantiser: inverse rotation (lower lanes
+// fetch cos, their partners sin, for the same indices), group abs-max,
+// scale, codes.  The cos/sin operands of all 8 steps are fetched first (one
+// round trip), then the values, then the steps run unrolled.  Codes go to
+// [T][G][K]; the scale of row r = 16 s + rr of the block goes to atom line
+// r % 32, word r / 32 (rows past T: 127; invalid position: zero codes,
+// scale 0).
+__device__ __forceinline__ void qslice_rope(const BmmArgs& p, const QJob& j, int s,
+                                            const uint8_t* buf, int lane, uint32_t badmask,
+                                            int64_t pl) {
+  const int hw = lane >> 4;
+  const int sub = lane & 15;
+  const int c = j.kg * 16 + sub;
+  const int t0 = j.t0 + kQRows * s;
+  const int first = 16 - (p.R >> 3);
+  const int dist = p.R >> 4;
+  const bool rope_lane = sub >= first;
+  const bool lower = sub < first + dist;
+  const int partner = (hw << 4) | (rope_lane ? (lower ? sub + dist : sub - dist) : sub);
+  const int i0 = (sub - first - (lower ? 0 : dist)) * 8;
+  const uint16_t* tab = lower ? p.cos_tab : p.sin_tab;
+  uint8_t* arow = p.qatoms + (size_t)j.f * kSfAtomBytes + (16 * (s & 1)) * 16 + (s >> 1) * 4;
+  uint4 cs[kQRows / 2];
+#pragma unroll
+  for (int i = 0; i < kQRows / 2; ++i) {
+    const int rr = 2 * i + hw;
+    const int64_t pp = __shfl_sync(0xffffffffu, (long long)pl, rr);
+    const bool rot = rope_lane && !((badmask >> rr) & 1u) && t0 + rr < p.T;
+    cs[i] = make_uint4(0, 0, 0, 0);
+    if (rot) cs[i] = __ldg(reinterpret_cast<const uint4*>(tab + pp * p.cs_ld + i0));
+  }
+  uint4 v[kQRows / 2];
+#pragma unroll
+  for (int i = 0; i < kQRows / 2; ++i)
+    v[i] = *reinterpret_cast<const uint4*>(buf + (2 * i + hw) * 256 + sub * 16);
+#pragma unroll
+  for (int i = 0; i < kQRows / 2; ++i) {
+    const int rr = 2 * i + hw;
+    const int t = t0 + rr;
+    const bool bad = (badmask >> rr) & 1u;
+    uint4 o, pv;
+    o.x = __shfl_sync(0xffffffffu, cs[i].x, partner);
+    o.y = __shfl_sync(0xffffffffu, cs[i].y, partner);
+    o.z = __shfl_sync(0xffffffffu, cs[i].z, partner);
+    o.w = __shfl_sync(0xffffffffu, cs[i].w, partner);
+    pv.x = __shfl_sync(0xffffffffu, v[i].x, partner);
+    pv.y = __shfl_sync(0xffffffffu, v[i].y, partner);
+    pv.z = __shfl_sync(0xffffffffu, v[i].z, partner);
+    pv.w = __shfl_sync(0xffffffffu, v[i].w, partner);
+    float y[8];
+    unpack8(v[i], y);
+    if (rope_lane && !bad && t < p.T) {
+      float xp[8];
+      unpack8(pv, xp);
+      inv_rope8(y, xp, lower ? cs[i] : o, lower ? o : cs[i], lower);
+    }
+    uint32_t sb;
+    uint2 q8 = encode8(y, half_warp_amax(y), &sb);
+    q8 = bad ? make_uint2(0, 0) : q8;
+    sb = bad ? 0u : sb;
+    if (c * 8 < p.K && t < p.T)
+      *reinterpret_cast<uint2*>(p.qcodes + ((size_t)t * p.G + j.g) * p.K + c * 8) = q8;
+    if (sub == 0) *reinterpret_cast<uint32_t*>(arow + rr * 16) = (t < p.T ? sb : 127u) * 0x01010101u;
+  }
+}
+
+// One quantising warp: its slices k = 0, 1, ... (slice n = k * kQWorkers + qw
+// of its CTA's sequence), in order from its own ring, each described by the
+// producer.  It waits only on its slices' copies.  A plain slice is
+// quantised with 8 lanes per row, 16 values per lane (elements [8 l, 8 l + 8)
+// and [64 + 8 l, 64 + 8 l + 8) of the row's group for lane l of the row's 8,
+// so each shared-memory read is 128 contiguous bytes per row) and four rows
+// per step: the values of all four steps are read into registers (then the
+// slot is released), the abs-max of every step is taken (the shuffle trees
+// interleave), then every step's scale and codes, and only then are the
+// codes stored, with the same arithmetic as the standalone quantiser.
+// Publication: every kQPublish slices (each of the first few, and the last)
+// the warp makes its earlier slices' writes visible at gpu scope and raises
+// their jobs' counters; it does so just before the current slice's stores,
+// so that the fence finds the earlier stores done.
+__device__ __forceinline__ void quant_worker(const BmmArgs& p, const uint8_t* qx, const QMeta* qm,
+                                             uint64_t* qfull, uint64_t* qempty, int u_first,
+                                             int u_step, int qw, int lane,
+                                             volatile int* abort_flag) {
+  const int r4 = lane >> 3;  // row of the step
+  const int l8 = lane & 7;   // the row's lane
+  // Slices of this CTA: kQSlices per job, the jobs of every unit it walks.
+  int total = 0;
+  for (int u = u_first; u < p.units; u += u_step) {
+    const Unit w = decode_unit<false, 256>(p, u);
+    const int r = (w.y0 / 256 + w.x0 / 256) % p.y_tiles;
+    if (r < p.KG) total += kQSlices * ((p.KG - r + p.y_tiles - 1) / p.y_tiles);
+  }
+  ptx::griddep_wait();  // the counters are cleared by preceding work
+  int pend[kQPublish];
+  int npend = 0;
+  auto publish = [&]() {
+    // The codes and atom words are read by other CTAs through TMA.
+    ptx::fence_proxy_async_global();
+    ptx::fence_acq_rel_gpu();
+    __syncwarp();
+    if (lane < npend) {
+      int f = pend[0];
+#pragma unroll
+      for (int i = 1; i < kQPublish; ++i)
+        if (lane == i) f = pend[i];
+      ptx::red_add_relaxed_gpu(p.qflags + f, 1u);
+    }
+    npend = 0;
+  };
+  bool stopped = false;
+  int k = 0;
+  for (; k * kQWorkers + qw < total; ++k) {
+    const int slot = qslot(qw, k);
+    const bool ok = !*abort_flag && ptx::mbar_wait_hint(&qfull[slot], (uint32_t)(k / kQRing) & 1u,
+                                                        kWaitLimitNs, kPipeHintNs);
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0 && !*abort_flag) watchdog(abort_flag, kWdEpilogue);
+      stopped = true;
+      break;
+    }
+    const QMeta* md = qm + slot;
+    QJob j;
+    j.g = md->g;
+    j.kg = md->kg;
+    j.t0 = md->t0;
+    j.f = md->f;
+    const int s = md->s;
+    const uint32_t badmask = md->bad;
+    const uint8_t* buf = qx + slot * kQSliceBytes;
+    const bool due = npend == kQPublish || (npend > 0 && k <= kQPublish);
+    if (p.R > 0 && j.kg == p.KG - 1) {
+      const int64_t pl = md->pos[lane & 15];
+      if (due) publish();
+      qslice_rope(p, j, s, buf, lane, badmask, pl);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&qempty[slot]);
+    } else {
+      const int t0 = j.t0 + kQRows * s;
+      uint4 va[4], vb[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint8_t* row = buf + (4 * i + r4) * 256 + l8 * 16;
+        va[i] = *reinterpret_cast<const uint4*>(row);
+        vb[i] = *reinterpret_cast<const uint4*>(row + 128);
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&qempty[slot]);  // the slice is in registers
+      float m[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float ya[8], yb[8];
+        unpack8(va[i], ya);
+        unpack8(vb[i], yb);
+        float mx = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx = fmaxf(mx, fmaxf(fabsf(ya[e]), fabsf(yb[e])));
+        m[i] = mx;
+      }
+#pragma unroll
+      for (int d = 4; d >= 1; d >>= 1)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], d));
+      uint2 qa[4], qb[4];
+      uint32_t sw[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float ya[8], yb[8];
+        unpack8(va[i], ya);
+        unpack8(vb[i], yb);
+        uint32_t sb;
+        qa[i] = encode8(ya, m[i], &sb);
+        qb[i] = encode8(yb, m[i], &sb);
+        const int rr = 4 * i + r4;
+        const bool bad = (badmask >> rr) & 1u;  // a token with an invalid position is zeroed
+        qa[i] = bad ? make_uint2(0, 0) : qa[i];
+        qb[i] = bad ? make_uint2(0, 0) : qb[i];
+        sw[i] = (t0 + rr < p.T ? (bad ? 0u : sb) : 127u) * 0x01010101u;  // past T: scale 127
+      }
+      if (due) publish();
+      // Codes [T][G][K] (rows past T and elements past K are not written) and
+      // atom words: row r = 16 s + 4 i + r4 of the block sits at line
+      // r % 32, word r / 32.
+      const int ca = j.kg * 128 + l8 * 8;
+      uint8_t* crow = p.qcodes + ((size_t)(t0 + r4) * p.G + j.g) * p.K + ca;
+      const size_t cstep = (size_t)4 * p.G * p.K;
+      uint8_t* arow =
+          p.qatoms + (size_t)j.f * kSfAtomBytes + (16 * (s & 1) + r4) * 16 + (s >> 1) * 4;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (t0 + 4 * i + r4 < p.T) {
+          if (ca < p.K) *reinterpret_cast<uint2*>(crow + i * cstep) = qa[i];
+          if (ca + 64 < p.K) *reinterpret_cast<uint2*>(crow + i * cstep + 64) = qb[i];
+        }
+        if (l8 == 0) *reinterpret_cast<uint32_t*>(arow + i * 64) = sw[i];
+      }
+    }
+    if (badmask != 0 && j.kg == 0 && lane == 0 && p.err_flag != nullptr)
+      atomicOr(p.err_flag, MXQ_DEVERR_POSITION);
+#pragma unroll
+    for (int i = 0; i < kQPublish; ++i)
+      if (i == npend) pend[i] = j.f;
+    ++npend;
+  }
+  if (!stopped && npend > 0) publish();
+}
+
+template <bool SWAP, bool FUSED, int BN, int NSTAGE, bool PAIR, bool QUANT>
+__global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::THREADS),
+                                  (Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::CTAS_PER_SM))
     bmm_a8w8_kernel(const __grid_constant__ CUtensorMap tm_act,
                     const __grid_constant__ CUtensorMap tm_w,
                     const __grid_constant__ CUtensorMap tm_wsf,
-                    const __grid_constant__ CUtensorMap tm_out, const BmmArgs p) {
-  using C = Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>;
+                    const __grid_constant__ CUtensorMap tm_out,
+                    const __grid_constant__ CUtensorMap tm_asf,
+                    const __grid_constant__ CUtensorMap tm_xq, const BmmArgs p) {
+  using C = Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -239,6 +654,8 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
   uint64_t* sf_full = acc_empty + 1;
   uint64_t* sf_empty = sf_full + 2;
   uint64_t* mma_done = sf_empty + 2;
+  uint64_t* qfull = mma_done + 1;  // quantising form only
+  uint64_t* qempty = qfull + kQSlots;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_SLOT);
   uint8_t* csf = smem + C::OFF_CSF;
   __shared__ int abort_shared;
@@ -264,8 +681,10 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
       // the activation producer's arrival after its scale atom.  Fused: one
       // arrival per quantising warp; the copies are tracked by `landed`.
       // Pair form: the even CTA's barrier also takes the odd CTA's scale-atom
-      // arrival and counts the bytes of both CTAs' copies.
-      ptx::mbar_init(&full[s], FUSED ? kEpiWarps : (PAIR ? 3 : 2));
+      // arrival and counts the bytes of both CTAs' copies; quantising pair
+      // form: the atoms are copied too, so only the even CTA's two producers
+      // arrive.
+      ptx::mbar_init(&full[s], FUSED ? kEpiWarps : (PAIR ? (QUANT ? 2 : 3) : 2));
       ptx::mbar_init(&empty[s], 1);
       ptx::mbar_init(&landed[s], 1);
     }
@@ -276,6 +695,11 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
       ptx::mbar_init(&sf_empty[b], 1);
     }
     ptx::mbar_init(mma_done, 1);
+    if (QUANT)
+      for (int i = 0; i < kQSlots; ++i) {
+        ptx::mbar_init(&qfull[i], 1);
+        ptx::mbar_init(&qempty[i], 1);
+      }
     abort_shared = 0;
     ptx::fence_barrier_init();
   }
@@ -283,6 +707,10 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
     ptx::prefetch_tmap(&tm_act);
     ptx::prefetch_tmap(&tm_w);
     if (PAIR) ptx::prefetch_tmap(&tm_wsf);
+    if (QUANT) {
+      ptx::prefetch_tmap(&tm_asf);
+      ptx::prefetch_tmap(&tm_xq);
+    }
   }
   if (warp == 1) {
     if constexpr (PAIR) {
@@ -425,7 +853,7 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
     // completes once the copies have landed, then drain.
     ptx::named_sync(1, 64);
     const int act_issued = *act_done;
-    if (lane == 0) {
+    if (lane == 0 && !(QUANT && rank != 0)) {
       for (int j = min(issued, act_issued); j < max(issued, act_issued); ++j) {
         if (PAIR && rank != 0)
           ptx::mbar_arrive_remote(lead_full + 8u * (uint32_t)(j % NSTAGE));
@@ -445,6 +873,89 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
       }
     }
     }
+  } else if (warp == kActWarp && QUANT) {
+    // ------------------------------- activation producer (quantising form)
+    // Per stage: the job counter of (this CTA's 128 tokens, K group) must
+    // show all quantising warps done; lanes 0 and 1 each poll the counters of
+    // the next few stages of the unit (one round trip for all of them) and
+    // fence once they see them complete, then lane 0 TMA-loads the codes and
+    // lane 1 the scale atom, both counted on the even CTA's stage barrier.
+    int it = 0;
+    bool stop = false;
+    ptx::griddep_wait();
+    for (int u = u_first; u < p.units && !stop; u += u_step) {
+      const Unit w = decode_unit<SWAP, BN>(p, u);
+      const int fbase = (w.g * p.MB + w.x0 / 128 + (int)rank) * p.KG + w.kg_begin;
+      int ready_end = 0;
+      for (int kk = 0; kk < w.nk; ++kk) {
+        const int s = it % NSTAGE;
+        const uint32_t ph = (uint32_t)(it / NSTAGE) & 1u;
+        // Every decision of this loop is taken warp-uniformly (the polls
+        // below use warp shuffles).
+        const bool ok_empty =
+            !*abort_flag && ptx::mbar_wait_hint(&empty[s], ph ^ 1u, kWaitLimitNs, kPipeHintNs);
+        if (!__all_sync(0xffffffffu, ok_empty)) {
+          if (lane == 0 && !*abort_flag) watchdog(abort_flag, kWdProducer);
+          stop = true;
+          break;
+        }
+        if (kk >= ready_end) {
+          const int win = min(8, w.nk - kk);
+          uint64_t t0 = 0;
+          int nready = 0;
+          while (true) {
+            int cnt = 0;
+            if (lane < 2) {
+              uint32_t fv[8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                fv[q] = q < win ? ptx::ld_relaxed_gpu(p.qflags + fbase + kk + q) : 0u;
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                if (cnt == q && fv[q] >= (uint32_t)kQSlices) cnt = q + 1;
+            }
+            nready = min(__shfl_sync(0xffffffffu, cnt, 0), __shfl_sync(0xffffffffu, cnt, 1));
+            if (nready > 0) break;
+            int give_up = 0;  // 1: another role aborted, 2: this wait ran out
+            if (lane == 0) {
+              const uint64_t now = ptx::globaltimer();
+              if (*abort_flag)
+                give_up = 1;
+              else if (t0 == 0)
+                t0 = now;
+              else if (now - t0 > kWaitLimitNs)
+                give_up = 2;
+            }
+            give_up = __shfl_sync(0xffffffffu, give_up, 0);
+            if (give_up) {
+              if (give_up == 2 && lane == 0) watchdog(abort_flag, kWdProducer);
+              stop = true;
+              break;
+            }
+            __nanosleep(kFlagPollNs);
+          }
+          if (stop) break;
+          if (lane < 2) {
+            ptx::fence_acq_rel_gpu();
+            ptx::fence_proxy_async_global();
+          }
+          ready_end = kk + nready;
+        }
+        const uint32_t bar = lead_full + 8u * (uint32_t)s;
+        if (lane == 0) {
+          if (rank == 0) ptx::mbar_arrive_expect_tx(&full[s], 2 * (C::X_TILE + C::SFX_BYTES));
+          ptx::tma_load_3d_pair(smem + C::OFF_X + s * C::X_TILE, &tm_act, bar, (w.kg_begin + kk) * 128,
+                                w.g, w.x0 + arow);
+        } else if (lane == 1) {
+          ptx::tma_load_2d_pair(smem + C::OFF_SFX + s * C::SFX_BYTES, &tm_asf, bar, 0,
+                                2 * (fbase + kk));
+        }
+        __syncwarp();
+        ++it;
+      }
+    }
+    if (lane == 0) *act_done = it;
+    ptx::named_sync(1, 64);
   } else if (warp == kActWarp) {
     // ------------------------------------------------- activation producer
     // (The fused form quantises in the epilogue warps; this warp idles.)
@@ -599,6 +1110,14 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>::THREADS),
     }
     __syncwarp();
     if (!ptx::mbar_wait(mma_done, 0, kWaitLimitNs)) watchdog(abort_flag, kWdDrain);
+  } else if (QUANT && warp == kQProducerWarp) {
+    // ------------------------------------------ activation slice producer
+    quant_producer(p, &tm_xq, smem + C::OFF_QX, reinterpret_cast<QMeta*>(smem + C::OFF_QM), qfull,
+                   qempty, u_first, u_step, (int)rank, lane, abort_flag);
+  } else if (QUANT && warp >= kQWarpHi) {
+    // ------------------------------------------------ quantising warps
+    quant_worker(p, smem + C::OFF_QX, reinterpret_cast<const QMeta*>(smem + C::OFF_QM), qfull, qempty,
+                 u_first, u_step, warp - kQWarpHi, lane, abort_flag);
   } else if (warp == 2) {
     // ------------------------------------------------- activation scales
     // (The fused form quantises in the epilogue warps and has no loader.)
@@ -1008,8 +1527,9 @@ bool encode_3d(CUtensorMap* m, const void* base, bool bf16, uint64_t d0, uint64_
   return r == CUDA_SUCCESS;
 }
 
-// 2-D uint8 map over the prepared weight scales, 256-byte rows (two per
-// 512-byte atom), boxes of `rows` rows: the pair form's scale-atom copies.
+// 2-D uint8 map over scale atoms (the prepared weight scales, or the
+// activation atoms of the quantising form), 256-byte rows (two per 512-byte
+// atom), boxes of `rows` rows: the pair form's scale-atom copies.
 bool encode_scale_rows(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
   auto enc = get_encode();
   if (!enc) return false;
@@ -1023,27 +1543,34 @@ bool encode_scale_rows(CUtensorMap* m, const void* base, uint64_t rows, uint32_t
   return r == CUDA_SUCCESS;
 }
 
-template <bool SWAP, bool FUSED, int BN, int NSTAGE, bool PAIR = false>
+template <bool SWAP, bool FUSED, int BN, int NSTAGE, bool PAIR = false, bool QUANT = false>
 cudaError_t launch_cfg(const void* a, const uint8_t* w, BmmArgs args, int num_sms,
                        cudaStream_t s, const char** why) {
-  using C = Cfg<SWAP, FUSED, BN, NSTAGE, PAIR>;
+  using C = Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>;
   const uint64_t K = args.K, G = args.G, T = args.T, N = args.N;
   CUtensorMap tm_act, tm_w;
   const uint32_t act_box = SWAP ? BN : C::BM;
   const uint32_t w_box = SWAP ? C::BM : C::Y_ROWS;
   const uint64_t esz = FUSED ? 2 : 1;  // fused form: x is BF16
-  CUtensorMap tm_wsf = {}, tm_out = {};
+  CUtensorMap tm_wsf = {}, tm_out = {}, tm_asf = {}, tm_xq = {};
   const uint64_t atoms = G * (uint64_t)args.KG * (uint64_t)args.NB;
   if (!encode_3d(&tm_act, a, FUSED, K, G, T, K * esz, G * K * esz, 128, 1, act_box) ||
       !encode_3d(&tm_w, w, false, K, N, G, K, N * K, 128, w_box, 1) ||
       (PAIR && !encode_scale_rows(&tm_wsf, args.w_sf, atoms * (kSfAtomBytes / 256),
                                   (uint32_t)(C::W_SF_BYTES / 256))) ||
       // Output [T][G][N] BF16, 32 x 32 boxes of one group (pair-form epilogue).
-      (PAIR && !encode_3d(&tm_out, args.out, true, N, G, T, N * 2, G * N * 2, 32, 1, 32))) {
+      (PAIR && !encode_3d(&tm_out, args.out, true, N, G, T, N * 2, G * N * 2, 32, 1, 32)) ||
+      // Activation scale atoms written by the quantising warps, as 256-byte
+      // rows (two per atom).
+      (QUANT && !encode_scale_rows(&tm_asf, args.qatoms,
+                                   G * (uint64_t)args.MB * (uint64_t)args.KG * (kSfAtomBytes / 256),
+                                   (uint32_t)(kSfAtomBytes / 256))) ||
+      // The BF16 activation [T][G][K], 32-row x 128-value slices.
+      (QUANT && !encode_3d(&tm_xq, args.xq, true, K, G, T, K * 2, G * K * 2, 128, 1, kQRows))) {
     *why = "cuTensorMapEncodeTiled failed (driver entry point missing or arguments rejected)";
     return cudaErrorInvalidValue;
   }
-  auto kern = bmm_a8w8_kernel<SWAP, FUSED, BN, NSTAGE, PAIR>;
+  auto kern = bmm_a8w8_kernel<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>;
   // The shared-memory opt-in is set once per device (a host-side call that
   // must not run inside stream capture, so the first call on a device should
   // happen before any capture).
@@ -1118,7 +1645,7 @@ cudaError_t launch_cfg(const void* a, const uint8_t* w, BmmArgs args, int num_sm
     grid = args.units < slots ? args.units : slots;
   }
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, tm_act, tm_w, tm_wsf, tm_out, args);
+  return cudaLaunchKernelEx(&cfg, kern, tm_act, tm_w, tm_wsf, tm_out, tm_asf, tm_xq, args);
 }
 
 }  // namespace
@@ -1180,6 +1707,46 @@ cudaError_t launch_wo_a_fused(const void* x, const int64_t* pos, const void* cos
   args.y_tiles = 1;
   if (T <= 16) return launch_cfg<true, true, 16, 4>(x, w, args, num_sms, s, why);
   return launch_cfg<true, true, 32, 3>(x, w, args, num_sms, s, why);
+}
+
+cudaError_t launch_wo_a_prefill(const void* x, const int64_t* pos, const void* cos, const void* sin,
+                                int64_t cs_ld, int64_t max_pos, int R, const uint8_t* w,
+                                const uint8_t* w_sf, void* out, int64_t T, int G, int N, int K,
+                                int32_t* err_flag, void* ws, int num_sms, cudaStream_t s,
+                                const char** why) {
+  BmmArgs args = {};
+  args.w_sf = w_sf;
+  args.out = reinterpret_cast<__nv_bfloat16*>(out);
+  args.T = (int)T;
+  args.G = G;
+  args.N = N;
+  args.K = K;
+  args.KG = (int)ceil_div(K, kGroup);
+  args.NB = (int)sf_row_blocks(N);
+  args.pos = pos;
+  args.cos_tab = reinterpret_cast<const uint16_t*>(cos);
+  args.sin_tab = reinterpret_cast<const uint16_t*>(sin);
+  args.cs_ld = cs_ld;
+  args.max_pos = max_pos;
+  args.R = R;
+  args.err_flag = err_flag;
+  args.x_span = 256;
+  args.x_tiles = (int)ceil_div(T, 256);
+  args.y_tiles = (int)ceil_div(N, 256);
+  args.splits = 1;
+  args.kg_per_split = args.KG;
+  args.MB = 2 * args.x_tiles;
+  const WoaPrefillLayout l = woa_prefill_layout(T, G, K);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  args.xq = reinterpret_cast<const uint16_t*>(x);
+  args.qcodes = base + l.codes;
+  args.qatoms = base + l.atoms;
+  args.qflags = reinterpret_cast<uint32_t*>(base + l.flags);
+  // The job counters start at zero on every call (a counter is raised once
+  // per quantising warp and job, and read against that count).
+  cudaError_t e = cudaMemsetAsync(args.qflags, 0, l.total - l.flags, s);
+  if (e != cudaSuccess) return e;
+  return launch_cfg<false, false, 256, 5, true, true>(args.qcodes, w, args, num_sms, s, why);
 }
 
 cudaError_t watchdog_read(uint32_t* value, bool clear) {

@@ -48,6 +48,34 @@ cudaError_t launch_wo_a_fused(const void* x, const int64_t* pos, const void* cos
                               const uint8_t* w_sf, void* out, int64_t T, int G, int N, int K,
                               int32_t* err_flag, int num_sms, cudaStream_t s, const char** why);
 
+// One-launch wo_a for T > 128 tokens: the CTA-pair GEMM with quantising
+// warps (inverse RoPE when R > 0) that fill the workspace `ws` (layout
+// below, woa_prefill_layout(T, G, K).total bytes, 256-byte aligned).
+constexpr int kPairMinTokens = 129;
+cudaError_t launch_wo_a_prefill(const void* x, const int64_t* pos, const void* cos, const void* sin,
+                                int64_t cs_ld, int64_t max_pos, int R, const uint8_t* w,
+                                const uint8_t* w_sf, void* out, int64_t T, int G, int N, int K,
+                                int32_t* err_flag, void* ws, int num_sms, cudaStream_t s,
+                                const char** why);
+
+// Workspace of launch_wo_a_prefill, each region 256-byte aligned: E4M3 codes
+// [T][G][K]; activation scale atoms [G][MB][KG][512] with MB = 2*ceil(T/256)
+// 128-token blocks and KG = ceil(K/128); job counters [G][MB][KG] uint32.
+struct WoaPrefillLayout {
+  size_t codes, atoms, flags, total;
+};
+inline size_t round_up_256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+inline WoaPrefillLayout woa_prefill_layout(int64_t T, int G, int K) {
+  const size_t MB = 2 * (size_t)ceil_div(T, 256);
+  const size_t jobs = (size_t)G * MB * (size_t)ceil_div(K, kGroup);
+  WoaPrefillLayout l;
+  l.codes = 0;
+  l.atoms = round_up_256((size_t)T * G * K);
+  l.flags = l.atoms + round_up_256(jobs * kSfAtomBytes);
+  l.total = l.flags + round_up_256(jobs * 4);
+  return l;
+}
+
 cudaError_t watchdog_read(uint32_t* value, bool clear);
 
 // One tiny kernel whose only wait can never be satisfied; it must give up

@@ -132,7 +132,14 @@ def test_wo_a_argument_errors(L):
     assert wo_a(L, T=0, x=None, out=None) == 0
     assert L.mxq_wo_a_workspace_bytes(32, 8, 4096, 1024) == 0
     assert L.mxq_wo_a_workspace_bytes(33, 8, 4096, 1024) == 33 * 8 * 4096 + 33 * 8 * 32
-    assert L.mxq_wo_a_workspace_bytes(8192, 8, 4096, 1024) == 8192 * 8 * 4096 + 8192 * 8 * 32
+    assert L.mxq_wo_a_workspace_bytes(128, 8, 4096, 1024) == 128 * 8 * 4096 + 128 * 8 * 32
+    # Above 128 tokens: codes [T, G, D], scale atoms [G, 2*ceil(T/256), ceil(D/128), 512] and
+    # job counters [G, 2*ceil(T/256), ceil(D/128)] uint32, each region rounded up to 256 bytes.
+    jobs = 8 * 64 * 32
+    assert L.mxq_wo_a_workspace_bytes(8192, 8, 4096, 1024) == 8192 * 8 * 4096 + jobs * 512 + jobs * 4
+    jobs = 3 * 6 * 5
+    assert L.mxq_wo_a_workspace_bytes(700, 3, 576, 1024) == (
+        (700 * 3 * 576 + 255) // 256 * 256 + jobs * 512 + (jobs * 4 + 255) // 256 * 256)
     assert wo_a(L, T=8192) == 6  # prefill sizes go through the workspace
 
 

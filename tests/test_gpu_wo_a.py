@@ -105,3 +105,110 @@ def test_out_of_range_position_in_one_launch(mxq):
     good = np.array([0, 2, 4, 5])
     a, sa = oracle_quant(x[good], pos[good], cos, sin, 64)
     check_gemm(out[good], *O.bmm_a8w8_ref(a, sa, w, sw), "good rows")
+
+
+# ----------------------------------------------------------------------------
+# Above 128 tokens mxq_wo_a is one launch of the CTA-pair GEMM whose extra
+# warps quantise the activation into the workspace: codes [T, G, D], scale
+# atoms [G, MB, KG, 512] (MB = 2 * ceil(T / 256) blocks of 128 tokens; row r of
+# a block holds its scale byte four times at (r % 32) * 16 + (r // 32) * 4) and
+# one uint32 job counter per (g, block, k group), raised once for each of the
+# 8 slices of 16 rows that the CTA owning the block quantises.
+
+def ws_layout(T, G, D):
+    r256 = lambda v: (v + 255) // 256 * 256
+    MB = 2 * ((T + 255) // 256)
+    KG = (D + 127) // 128
+    jobs = G * MB * KG
+    atoms = r256(T * G * D)
+    flags = atoms + r256(jobs * 512)
+    return atoms, flags, flags + r256(jobs * 4), MB, KG
+
+
+def atom_scales(ws, T, G, D):
+    """Scale bytes [T, G, KG] read back from the workspace's atoms (each word must
+    hold one byte four times; rows past T must hold 127)."""
+    atoms, flags, _, MB, KG = ws_layout(T, G, D)
+    at = ws[atoms:atoms + G * MB * KG * 512].cpu().numpy().reshape(G, MB, KG, 32, 4, 4)
+    assert (at == at[..., :1]).all(), "an atom word does not repeat its byte"
+    # [G, MB, KG, line r%32, word r//32] -> [G, MB, r, KG]
+    b = at[..., 0].transpose(0, 1, 4, 3, 2).reshape(G, MB * 128, KG)
+    assert (b[:, T:, :] == 127).all()
+    return b[:, :T, :].transpose(1, 0, 2)
+
+
+@pytest.mark.parametrize("T,G,D,N,R", [
+    (129, 1, 256, 16, 64),      # one token in the second pair half
+    (257, 2, 512, 272, 16),     # odd CTA of the second block almost empty
+    (300, 3, 640, 1040, 128),   # five weight tiles, the last mostly past N
+    (1000, 2, 1024, 256, 64),   # one weight tile: each pair quantises all K groups
+    (384, 2, 576, 512, 0),      # unaligned K (4 groups + 64), no rotation
+    (520, 1, 2304, 768, 0),     # unaligned K (18 groups), three weight tiles
+])
+def test_pair_quant_workspace_and_output(mxq, T, G, D, N, R):
+    x, pos, cos, sin = wo_a_inputs(T, G, D, N, max(R, 16), seed=1900 + T + D, max_pos=5000)
+    w, sw = oracle_weights(G, N, D, seed=1901 + D)
+    xd, pd, cd, sd, wd, swd = to_dev(x, pos, cos, sin, w, sw)
+    wsf = mxq.mxq_prepare_weight_scales(swd, D)
+    atoms, flags, total, MB, KG = ws_layout(T, G, D)
+    assert mxq.mxq_wo_a_workspace_bytes(T, G, D, N) == total
+    ws = torch.full((total,), 0xA5, dtype=torch.uint8, device="cuda")
+    out = mxq.mxq_wo_a(xd, pd, cd, sd, wd, wsf, R=R, ws=ws)
+    torch.cuda.synchronize()
+    a, sa = oracle_quant(x, pos, cos, sin, R)
+    codes = ws[:T * G * D].cpu().numpy().reshape(T, G, D)
+    assert np.array_equal(codes, a), "codes differ from the oracle"
+    assert np.array_equal(atom_scales(ws, T, G, D), sa), "scale bytes differ from the oracle"
+    cnt = ws[flags:flags + G * MB * KG * 4].cpu().view(torch.int32).numpy()
+    assert (cnt == 8).all(), "a job counter is not 8"
+    check_gemm(out, *O.bmm_a8w8_ref(a, sa, w, sw), f"pair quant T={T} D={D} N={N} R={R}")
+    # Same operands, same MMA sequence: bit-identical to quantiser + GEMM.
+    q, sc = mxq.mxq_inv_rope_group_quant(xd, pd, cd, sd, R)
+    out2 = mxq.mxq_bmm_a8w8(q, sc, wd, wsf)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2)
+
+
+def test_pair_quant_out_of_range_positions(mxq):
+    T, G, D, N = 300, 2, 512, 256
+    x, _, cos, sin = wo_a_inputs(T, G, D, N, 64, seed=2000, max_pos=100, max_pos_table=100)
+    rng = np.random.Generator(np.random.PCG64(2001))
+    pos = torch.from_numpy(rng.integers(0, 100, T).astype(np.int64))
+    bad = np.array([0, 5, 128, 200, 299])
+    pos[bad] = torch.tensor([-1, 100, 1000, -7, 100], dtype=torch.int64)
+    w, sw = oracle_weights(G, N, D, seed=2002)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, _ = run(mxq, x, pos, cos, sin, w, sw, 64, err=err)
+    assert int(err.item()) == mxq.MXQ_DEVERR_POSITION
+    o = out.float().cpu()
+    assert (o[bad] == 0).all()
+    good = np.setdiff1d(np.arange(T), bad)
+    a, sa = oracle_quant(x[good], pos[good], cos, sin, 64)
+    check_gemm(out[good], *O.bmm_a8w8_ref(a, sa, w, sw), "good rows")
+
+
+def test_pair_quant_deterministic_and_graph_replay(mxq):
+    """Repeated calls, eager and replayed from a CUDA graph (the counters are
+    cleared inside each call), give identical outputs."""
+    T, G, D, N = 700, 4, 1024, 512
+    x, pos, cos, sin = wo_a_inputs(T, G, D, N, 64, seed=2100, max_pos=4096)
+    w, sw = oracle_weights(G, N, D, seed=2101)
+    out, (xd, pd, cd, sd, wd, wsf) = run(mxq, x, pos, cos, sin, w, sw, 64)
+    ws = torch.empty(mxq.mxq_wo_a_workspace_bytes(T, G, D, N), dtype=torch.uint8, device="cuda")
+    o2 = torch.empty_like(out)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        mxq.mxq_wo_a(xd, pd, cd, sd, wd, wsf, R=64, out=o2, ws=ws, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert torch.equal(out, o2)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        mxq.mxq_wo_a(xd, pd, cd, sd, wd, wsf, R=64, out=o2, ws=ws,
+                     stream=torch.cuda.current_stream())
+    for _ in range(3):
+        o2.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, o2)
