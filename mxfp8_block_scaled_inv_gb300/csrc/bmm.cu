@@ -100,25 +100,27 @@ constexpr int kEpiWarp0 = 3;   // epilogue warps 3-10
 constexpr int kEpiWarps = 8;
 constexpr int kActWarp = 11;   // activation producer (unfused forms)
 constexpr int kGateWarp = 12;  // pair form: waits on the MMA warp's barriers
-// Quantising pair form: warp 2 loads the BF16 activation slices (16 rows x
-// 128 values, 4 KB) with TMA, and warps 13-15 quantise them, slice n going to
-// warp n % kQWorkers; each of those warps owns a ring of kQRing slots that it
-// consumes in order.  A job (128 rows of one K group) is kQSlices slices and
-// its counter reaches kQSlices.
-constexpr int kQProducerWarp = 2;
-constexpr int kQWarpHi = 13;
-constexpr int kQWorkers = 3;
+// Quantising pair form: a job (128 rows of one K group) is kQSlices slices
+// of 16 rows x 128 values, and epilogue warp w quantises slice w of every
+// job of its CTA, between accumulator drains, from its own shared-memory slot
+// that it refills itself with TMA; a job's counter reaches kQSlices.
+constexpr int kQWorkers = kEpiWarps;
 constexpr int kQSlices = 8;
 constexpr int kQRows = 128 / kQSlices;
 constexpr int kQSliceBytes = kQRows * 128 * 2;
-constexpr int kQRing = 3;
-constexpr int kQSlots = kQWorkers * kQRing;
-constexpr int kQMetaBytes = 32 + 8 * kQRows;
-// Longest sleep between two polls of a not-yet-published counter.
+constexpr int kQSlots = kQWorkers;
+static_assert(kQSlices == kQWorkers, "one slice of every job per epilogue warp");
+// Longest sleep between two polls of a not-yet-published counter, and
+// between two polls of an epilogue warp with nothing ready.
 constexpr uint32_t kFlagPollNs = 128;
-// Publications are batched: the gpu-scope fence waits for every store the
-// warp still has in flight.
-constexpr int kQPublish = 8;
+constexpr uint32_t kEpiPollNs = 32;
+// Each quantising warp prefetches its slice of the job this many jobs ahead
+// into L2 (its shared-memory copies then wait on L2, not DRAM).
+constexpr int kQPrefetch = 4;
+// Publications are batched (and made at once whenever the warp has nothing
+// else ready): the gpu-scope fence waits for every store the warp still has
+// in flight.
+constexpr int kQPublish = 4;
 
 struct BmmArgs {
   const uint8_t* a_sf;  // [T][G][KG]
@@ -187,12 +189,10 @@ struct Cfg {
   // Quantising form: the BF16 activation slices.
   static constexpr int QX_BYTES = QUANT ? kQSlots * kQSliceBytes : 0;
   static constexpr int OFF_QX = OFF_OUT + OUT_BYTES;
-  static constexpr int QM_BYTES = QUANT ? kQSlots * kQMetaBytes : 0;  // slice descriptions
-  static constexpr int OFF_QM = OFF_QX + QX_BYTES;
-  static constexpr int OFF_BAR = OFF_QM + QM_BYTES;
+  static constexpr int OFF_BAR = OFF_QX + QX_BYTES;
   // full[NSTAGE], empty[NSTAGE], landed[NSTAGE], acc_full, acc_empty,
-  // sf_full[2], sf_empty[2], mma_done, then qfull[kQSlots], qempty[kQSlots]
-  static constexpr int N_BARS = 3 * NSTAGE + 7 + (QUANT ? 2 * kQSlots : 0);
+  // sf_full[2], sf_empty[2], mma_done, then qfull[kQSlots]
+  static constexpr int N_BARS = 3 * NSTAGE + 7 + (QUANT ? kQSlots : 0);
   static constexpr int OFF_SLOT = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_SLOT + 16 + 1024;
   // Two CTAs share an SM when their shared memory allows it (the small-token
@@ -212,9 +212,9 @@ struct Cfg {
   // The pair form adds a gate warp that does the MMA warp's barrier waits:
   // the tensor pipe's instruction queue is shallow, so any wait in the
   // issuing warp between stages leaves the pipe idle.
-  // The quantising pair form adds the quantising warps (warp 2, the scale
-  // loader otherwise, loads their slices).
-  static constexpr int THREADS = (FUSED ? 11 : (PAIR ? (QUANT ? kQWarpHi + kQWorkers : 13) : 12)) * 32;
+  // (In the quantising pair form warp 2, the scale loader otherwise, loads
+  // the activation slices.)
+  static constexpr int THREADS = (FUSED ? 11 : (PAIR ? 13 : 12)) * 32;
   // Instruction descriptor, kind::mxf8f6f4 with block scaling: E4M3 A and
   // B (format 0), both K-major, N >> 3 at bits 17-22, UE8M0 scale type at
   // bit 23, M >> 4 at bits 24-28, scale-factor ids 0.
@@ -322,108 +322,6 @@ __device__ __forceinline__ bool qjob_first(const BmmArgs& p, int u_first, int u_
   return false;
 }
 
-// Slot of the k-th slice of quantising warp w (its own ring, used in order).
-__device__ __forceinline__ int qslot(int w, int k) { return w * kQRing + k % kQRing; }
-
-// Description of the slice in a slot, written by the producer beside the
-// copy (the quantising warps then need no job walk and no position loads).
-struct QMeta {
-  int g, kg, t0, f;           // job fields (t0 = the block's first token)
-  int s;                      // slice within the job
-  uint32_t bad;               // bit r: row r has an invalid position
-  int pad[2];
-  int64_t pos[kQRows];        // positions of the rows (0 past T, or without RoPE)
-};
-static_assert(sizeof(QMeta) == kQMetaBytes, "slice description size");
-
-// Producer: slices in order, two per round (lanes 0 and 1 each issue one
-// copy: a thread issues only about one TMA copy every few hundred cycles;
-// lanes 16 h + r describe row r of the round's slice h).  Slice n is the
-// (n / kQWorkers)-th slice of warp n % kQWorkers; its slot is refilled once
-// that warp has released the slice kQRing before it.  The positions of the
-// next round are loaded while this one waits.
-__device__ __forceinline__ void quant_producer(const BmmArgs& p, const CUtensorMap* tm_x,
-                                               uint8_t* qx, QMeta* qm, uint64_t* qfull,
-                                               uint64_t* qempty, int u_first, int u_step, int rank,
-                                               int lane, volatile int* abort_flag) {
-  QJob j;
-  if (!qjob_first(p, u_first, u_step, rank, j)) return;
-  ptx::griddep_wait();  // x and the positions come from preceding work
-  const int half = lane >> 4;
-  const int row = lane & 15;
-  auto pos_of = [&](const QJob& jj, int sl) -> int64_t {
-    const int t = jj.t0 + kQRows * sl + row;
-    return (p.R > 0 && t < p.T) ? __ldg(p.pos + t) : 0;
-  };
-  int s = 0;
-  int64_t pcur = pos_of(j, half);
-  int n = 0;
-  while (true) {
-    QJob j2 = j;
-    int s2 = s + 2;
-    bool more = true;
-    if (s2 == kQSlices) {
-      s2 = 0;
-      more = qjob_next(p, u_step, rank, j2);
-    }
-    const int64_t pnext = more ? pos_of(j2, s2 + half) : 0;
-    bool ok = !*abort_flag;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int m = n + h;
-      const int k = m / kQWorkers;
-      if (ok && k >= kQRing)
-        ok = ptx::mbar_wait_hint(&qempty[qslot(m % kQWorkers, k)],
-                                 (uint32_t)((k / kQRing) - 1) & 1u, kWaitLimitNs, kPipeHintNs);
-    }
-    if (!__all_sync(0xffffffffu, ok)) {
-      if (lane == 0 && !*abort_flag) watchdog(abort_flag, kWdLoader);
-      break;
-    }
-    {
-      const int t = j.t0 + kQRows * (s + half) + row;
-      const bool bad = p.R > 0 && t < p.T && (pcur < 0 || pcur >= p.max_pos);
-      const uint32_t bm = __ballot_sync(0xffffffffu, bad);
-      const int m = n + half;
-      QMeta* md = qm + qslot(m % kQWorkers, m / kQWorkers);
-      md->pos[row] = pcur;
-      if (row == 0) {
-        md->g = j.g;
-        md->kg = j.kg;
-        md->t0 = j.t0;
-        md->f = j.f;
-        md->s = s + half;
-        md->bad = (bm >> (16 * half)) & 0xFFFFu;
-      }
-    }
-    __syncwarp();  // the descriptions are written before the copies' arrivals
-    if (lane < 2) {
-      const int m = n + lane;
-      const int slot = qslot(m % kQWorkers, m / kQWorkers);
-      ptx::mbar_arrive_expect_tx(&qfull[slot], kQSliceBytes);
-      ptx::tma_load_3d(qx + slot * kQSliceBytes, tm_x, &qfull[slot], j.kg * 128, j.g,
-                       j.t0 + kQRows * (s + lane));
-    }
-    __syncwarp();
-    n += 2;
-    pcur = pnext;
-    if (!more) break;
-    j = j2;
-    s = s2;
-  }
-  // Every issued copy lands before the CTA may retire (the quantising warps
-  // consume them all unless a wait ran out): the last issued slice of every
-  // slot, whose phase is the slot's latest.
-  for (int m = max(0, n - kQSlots); m < n; ++m) {
-    const int k = m / kQWorkers;
-    if (!ptx::mbar_wait(&qfull[qslot(m % kQWorkers, k)], (uint32_t)(k / kQRing) & 1u,
-                        kWaitLimitNs)) {
-      if (lane == 0) watchdog(abort_flag, kWdDrain);
-      break;
-    }
-  }
-}
-
 // Quantises a rotated slice (the row's last group when R > 0; one in KG
 // jobs): steps of two rows, a half-warp per row and 8 values per lane, with
 // the arithmetic of the standalone quantiser: inverse rotation (lower lanes
@@ -492,145 +390,76 @@ __device__ __forceinline__ void qslice_rope(const BmmArgs& p, const QJob& j, int
   }
 }
 
-// One quantising warp: its slices k = 0, 1, ... (slice n = k * kQWorkers + qw
-// of its CTA's sequence), in order from its own ring, each described by the
-// producer.  It waits only on its slices' copies.  A plain slice is
-// quantised with 8 lanes per row, 16 values per lane (elements [8 l, 8 l + 8)
-// and [64 + 8 l, 64 + 8 l + 8) of the row's group for lane l of the row's 8,
-// so each shared-memory read is 128 contiguous bytes per row) and four rows
-// per step: the values of all four steps are read into registers (then the
-// slot is released), the abs-max of every step is taken (the shuffle trees
-// interleave), then every step's scale and codes, and only then are the
-// codes stored, with the same arithmetic as the standalone quantiser.
-// Publication: every kQPublish slices (each of the first few, and the last)
-// the warp makes its earlier slices' writes visible at gpu scope and raises
-// their jobs' counters; it does so just before the current slice's stores,
-// so that the fence finds the earlier stores done.
-__device__ __forceinline__ void quant_worker(const BmmArgs& p, const uint8_t* qx, const QMeta* qm,
-                                             uint64_t* qfull, uint64_t* qempty, int u_first,
-                                             int u_step, int qw, int lane,
-                                             volatile int* abort_flag) {
+// Quantises a plain slice from its slot: 8 lanes per row, 16 values per
+// lane (elements [8 l, 8 l + 8) and [64 + 8 l, 64 + 8 l + 8) of the row's
+// group for lane l of the row's 8, so each shared-memory read is 128
+// contiguous bytes per row), four rows per step.  The values of all four
+// steps are read into registers and the slot is released (`release`), then
+// the abs-max of every step is taken (the shuffle trees interleave), then
+// every step's scale and codes, then `before_stores` runs and the codes and
+// atom words are stored, with the same arithmetic as the standalone
+// quantiser.  Rows past T: no codes, scale 127; rows with an invalid
+// position: zero codes, scale 0; row r = 16 s + 4 i + r4 of the block sits
+// at atom line r % 32, word r / 32.
+template <class Release, class BeforeStores>
+__device__ __forceinline__ void qslice_plain(const BmmArgs& p, const QJob& j, int s,
+                                             const uint8_t* buf, int lane, uint32_t badmask,
+                                             Release&& release, BeforeStores&& before_stores) {
   const int r4 = lane >> 3;  // row of the step
   const int l8 = lane & 7;   // the row's lane
-  // Slices of this CTA: kQSlices per job, the jobs of every unit it walks.
-  int total = 0;
-  for (int u = u_first; u < p.units; u += u_step) {
-    const Unit w = decode_unit<false, 256>(p, u);
-    const int r = (w.y0 / 256 + w.x0 / 256) % p.y_tiles;
-    if (r < p.KG) total += kQSlices * ((p.KG - r + p.y_tiles - 1) / p.y_tiles);
+  const int t0 = j.t0 + kQRows * s;
+  uint4 va[4], vb[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint8_t* row = buf + (4 * i + r4) * 256 + l8 * 16;
+    va[i] = *reinterpret_cast<const uint4*>(row);
+    vb[i] = *reinterpret_cast<const uint4*>(row + 128);
   }
-  ptx::griddep_wait();  // the counters are cleared by preceding work
-  int pend[kQPublish];
-  int npend = 0;
-  auto publish = [&]() {
-    // The codes and atom words are read by other CTAs through TMA.
-    ptx::fence_proxy_async_global();
-    ptx::fence_acq_rel_gpu();
-    __syncwarp();
-    if (lane < npend) {
-      int f = pend[0];
+  release();
+  float m[4];
 #pragma unroll
-      for (int i = 1; i < kQPublish; ++i)
-        if (lane == i) f = pend[i];
-      ptx::red_add_relaxed_gpu(p.qflags + f, 1u);
-    }
-    npend = 0;
-  };
-  bool stopped = false;
-  int k = 0;
-  for (; k * kQWorkers + qw < total; ++k) {
-    const int slot = qslot(qw, k);
-    const bool ok = !*abort_flag && ptx::mbar_wait_hint(&qfull[slot], (uint32_t)(k / kQRing) & 1u,
-                                                        kWaitLimitNs, kPipeHintNs);
-    if (!__all_sync(0xffffffffu, ok)) {
-      if (lane == 0 && !*abort_flag) watchdog(abort_flag, kWdEpilogue);
-      stopped = true;
-      break;
-    }
-    const QMeta* md = qm + slot;
-    QJob j;
-    j.g = md->g;
-    j.kg = md->kg;
-    j.t0 = md->t0;
-    j.f = md->f;
-    const int s = md->s;
-    const uint32_t badmask = md->bad;
-    const uint8_t* buf = qx + slot * kQSliceBytes;
-    const bool due = npend == kQPublish || (npend > 0 && k <= kQPublish);
-    if (p.R > 0 && j.kg == p.KG - 1) {
-      const int64_t pl = md->pos[lane & 15];
-      if (due) publish();
-      qslice_rope(p, j, s, buf, lane, badmask, pl);
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&qempty[slot]);
-    } else {
-      const int t0 = j.t0 + kQRows * s;
-      uint4 va[4], vb[4];
+  for (int i = 0; i < 4; ++i) {
+    float ya[8], yb[8];
+    unpack8(va[i], ya);
+    unpack8(vb[i], yb);
+    float mx = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint8_t* row = buf + (4 * i + r4) * 256 + l8 * 16;
-        va[i] = *reinterpret_cast<const uint4*>(row);
-        vb[i] = *reinterpret_cast<const uint4*>(row + 128);
-      }
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&qempty[slot]);  // the slice is in registers
-      float m[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float ya[8], yb[8];
-        unpack8(va[i], ya);
-        unpack8(vb[i], yb);
-        float mx = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx = fmaxf(mx, fmaxf(fabsf(ya[e]), fabsf(yb[e])));
-        m[i] = mx;
-      }
-#pragma unroll
-      for (int d = 4; d >= 1; d >>= 1)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], d));
-      uint2 qa[4], qb[4];
-      uint32_t sw[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float ya[8], yb[8];
-        unpack8(va[i], ya);
-        unpack8(vb[i], yb);
-        uint32_t sb;
-        qa[i] = encode8(ya, m[i], &sb);
-        qb[i] = encode8(yb, m[i], &sb);
-        const int rr = 4 * i + r4;
-        const bool bad = (badmask >> rr) & 1u;  // a token with an invalid position is zeroed
-        qa[i] = bad ? make_uint2(0, 0) : qa[i];
-        qb[i] = bad ? make_uint2(0, 0) : qb[i];
-        sw[i] = (t0 + rr < p.T ? (bad ? 0u : sb) : 127u) * 0x01010101u;  // past T: scale 127
-      }
-      if (due) publish();
-      // Codes [T][G][K] (rows past T and elements past K are not written) and
-      // atom words: row r = 16 s + 4 i + r4 of the block sits at line
-      // r % 32, word r / 32.
-      const int ca = j.kg * 128 + l8 * 8;
-      uint8_t* crow = p.qcodes + ((size_t)(t0 + r4) * p.G + j.g) * p.K + ca;
-      const size_t cstep = (size_t)4 * p.G * p.K;
-      uint8_t* arow =
-          p.qatoms + (size_t)j.f * kSfAtomBytes + (16 * (s & 1) + r4) * 16 + (s >> 1) * 4;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (t0 + 4 * i + r4 < p.T) {
-          if (ca < p.K) *reinterpret_cast<uint2*>(crow + i * cstep) = qa[i];
-          if (ca + 64 < p.K) *reinterpret_cast<uint2*>(crow + i * cstep + 64) = qb[i];
-        }
-        if (l8 == 0) *reinterpret_cast<uint32_t*>(arow + i * 64) = sw[i];
-      }
-    }
-    if (badmask != 0 && j.kg == 0 && lane == 0 && p.err_flag != nullptr)
-      atomicOr(p.err_flag, MXQ_DEVERR_POSITION);
-#pragma unroll
-    for (int i = 0; i < kQPublish; ++i)
-      if (i == npend) pend[i] = j.f;
-    ++npend;
+    for (int e = 0; e < 8; ++e) mx = fmaxf(mx, fmaxf(fabsf(ya[e]), fabsf(yb[e])));
+    m[i] = mx;
   }
-  if (!stopped && npend > 0) publish();
+#pragma unroll
+  for (int d = 4; d >= 1; d >>= 1)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], d));
+  uint2 qa[4], qb[4];
+  uint32_t sw[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float ya[8], yb[8];
+    unpack8(va[i], ya);
+    unpack8(vb[i], yb);
+    uint32_t sb;
+    qa[i] = encode8(ya, m[i], &sb);
+    qb[i] = encode8(yb, m[i], &sb);
+    const int rr = 4 * i + r4;
+    const bool bad = (badmask >> rr) & 1u;
+    qa[i] = bad ? make_uint2(0, 0) : qa[i];
+    qb[i] = bad ? make_uint2(0, 0) : qb[i];
+    sw[i] = (t0 + rr < p.T ? (bad ? 0u : sb) : 127u) * 0x01010101u;
+  }
+  before_stores();
+  const int ca = j.kg * 128 + l8 * 8;
+  uint8_t* crow = p.qcodes + ((size_t)(t0 + r4) * p.G + j.g) * p.K + ca;
+  const size_t cstep = (size_t)4 * p.G * p.K;
+  uint8_t* arow = p.qatoms + (size_t)j.f * kSfAtomBytes + (16 * (s & 1) + r4) * 16 + (s >> 1) * 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (t0 + 4 * i + r4 < p.T) {
+      if (ca < p.K) *reinterpret_cast<uint2*>(crow + i * cstep) = qa[i];
+      if (ca + 64 < p.K) *reinterpret_cast<uint2*>(crow + i * cstep + 64) = qb[i];
+    }
+    if (l8 == 0) *reinterpret_cast<uint32_t*>(arow + i * 64) = sw[i];
+  }
 }
 
 template <bool SWAP, bool FUSED, int BN, int NSTAGE, bool PAIR, bool QUANT>
@@ -654,8 +483,7 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
   uint64_t* sf_full = acc_empty + 1;
   uint64_t* sf_empty = sf_full + 2;
   uint64_t* mma_done = sf_empty + 2;
-  uint64_t* qfull = mma_done + 1;  // quantising form only
-  uint64_t* qempty = qfull + kQSlots;
+  uint64_t* qfull = mma_done + 1;  // quantising form only: the epilogue warps' slots
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_SLOT);
   uint8_t* csf = smem + C::OFF_CSF;
   __shared__ int abort_shared;
@@ -696,10 +524,7 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
     }
     ptx::mbar_init(mma_done, 1);
     if (QUANT)
-      for (int i = 0; i < kQSlots; ++i) {
-        ptx::mbar_init(&qfull[i], 1);
-        ptx::mbar_init(&qempty[i], 1);
-      }
+      for (int i = 0; i < kQSlots; ++i) ptx::mbar_init(&qfull[i], 1);
     abort_shared = 0;
     ptx::fence_barrier_init();
   }
@@ -876,10 +701,11 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
   } else if (warp == kActWarp && QUANT) {
     // ------------------------------- activation producer (quantising form)
     // Per stage: the job counter of (this CTA's 128 tokens, K group) must
-    // show all quantising warps done; lanes 0 and 1 each poll the counters of
-    // the next few stages of the unit (one round trip for all of them) and
-    // fence once they see them complete, then lane 0 TMA-loads the codes and
-    // lane 1 the scale atom, both counted on the even CTA's stage barrier.
+    // show every slice quantised.  Lane i reads (acquire) the counter of the
+    // i-th next stage of the unit (one round trip for up to 32 stages; an
+    // acquire load, unlike a fence, does not wait for the copies this warp
+    // has in flight); lane 0 TMA-loads the codes and lane 1 the scale atom,
+    // both counted on the even CTA's stage barrier.
     int it = 0;
     bool stop = false;
     ptx::griddep_wait();
@@ -900,21 +726,14 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
           break;
         }
         if (kk >= ready_end) {
-          const int win = min(8, w.nk - kk);
+          const int win = min(32, w.nk - kk);
           uint64_t t0 = 0;
           int nready = 0;
           while (true) {
-            int cnt = 0;
-            if (lane < 2) {
-              uint32_t fv[8];
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                fv[q] = q < win ? ptx::ld_relaxed_gpu(p.qflags + fbase + kk + q) : 0u;
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                if (cnt == q && fv[q] >= (uint32_t)kQSlices) cnt = q + 1;
-            }
-            nready = min(__shfl_sync(0xffffffffu, cnt, 0), __shfl_sync(0xffffffffu, cnt, 1));
+            const bool rdy = lane < win && ptx::ld_acquire_gpu(p.qflags + fbase + kk + lane) >=
+                                               (uint32_t)kQSlices;
+            const uint32_t mask = __ballot_sync(0xffffffffu, rdy);
+            nready = mask == 0xffffffffu ? 32 : __ffs(~mask) - 1;  // ready stages in a row
             if (nready > 0) break;
             int give_up = 0;  // 1: another role aborted, 2: this wait ran out
             if (lane == 0) {
@@ -935,10 +754,10 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
             __nanosleep(kFlagPollNs);
           }
           if (stop) break;
-          if (lane < 2) {
-            ptx::fence_acq_rel_gpu();
-            ptx::fence_proxy_async_global();
-          }
+          // Each lane acquired its own stage's counter; the issuing lanes
+          // order their copies after the warp's loads.
+          __syncwarp();
+          if (lane < 2) ptx::fence_proxy_async_global();
           ready_end = kk + nready;
         }
         const uint32_t bar = lead_full + 8u * (uint32_t)s;
@@ -1110,18 +929,10 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
     }
     __syncwarp();
     if (!ptx::mbar_wait(mma_done, 0, kWaitLimitNs)) watchdog(abort_flag, kWdDrain);
-  } else if (QUANT && warp == kQProducerWarp) {
-    // ------------------------------------------ activation slice producer
-    quant_producer(p, &tm_xq, smem + C::OFF_QX, reinterpret_cast<QMeta*>(smem + C::OFF_QM), qfull,
-                   qempty, u_first, u_step, (int)rank, lane, abort_flag);
-  } else if (QUANT && warp >= kQWarpHi) {
-    // ------------------------------------------------ quantising warps
-    quant_worker(p, smem + C::OFF_QX, reinterpret_cast<const QMeta*>(smem + C::OFF_QM), qfull, qempty,
-                 u_first, u_step, warp - kQWarpHi, lane, abort_flag);
   } else if (warp == 2) {
     // ------------------------------------------------- activation scales
-    // (The fused form quantises in the epilogue warps and has no loader.)
-    if constexpr (!FUSED) {
+    // (The fused and quantising forms need no loader.)
+    if constexpr (!FUSED && !QUANT) {
     int ci = 0;
     bool stop = false;
     for (int u = u_first; u < p.units && !stop; u += u_step) {
@@ -1209,6 +1020,48 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + h * C::HALF;
     float* red = reinterpret_cast<float*>(smem + C::OFF_RED);  // split-K receive buffer
     int ti = 0;
+    // Pair form: drains this warp's quarter of the unit's accumulator (after
+    // its acc_full phase) and stores it.
+    auto pair_drain = [&](const Unit& w) {
+      // Drain 32 columns at a time and keep them as packed BF16 pairs (RNE,
+      // as in the other forms), so that the 13-warp CTA fits its register
+      // budget; the accumulator is released as soon as it is read.
+      uint32_t pk[C::HALF / 2];
+#pragma unroll
+      for (int c = 0; c < C::HALF / 32; ++c) {
+        uint32_t t32[32];
+        ptx::tmem_ld_32x32b_x32(trow + c * 32, t32);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[c * 16 + j] = pack_bf16x2(t32[2 * j], t32[2 * j + 1]);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0)  // the accumulator may be overwritten now
+        ptx::mbar_arrive_remote(ptx::map_shared_rank(ptx::smem_u32(acc_empty), 0));
+      // Rows of a lane are 16 KB apart in the output, so each warp stages
+      // 32 rows x 32 columns in shared memory and one lane stores the box
+      // with TMA (full lines, no per-lane scattered stores; rows past T
+      // and columns past N are clipped by the copy).
+      const int c0 = h * C::HALF;
+      uint8_t* buf = smem + C::OFF_OUT + (warp - kEpiWarp0) * C::OUT_TILE;
+#pragma unroll
+      for (int c = 0; c < C::HALF / 32; ++c) {
+        if (lane == 0) ptx::bulk_wait_read<0>();  // the previous chunk's store has read it
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(buf + lane * 64 + j * 16) =
+              make_uint4(pk[c * 16 + j * 4 + 0], pk[c * 16 + j * 4 + 1], pk[c * 16 + j * 4 + 2],
+                         pk[c * 16 + j * 4 + 3]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_3d(&tm_out, buf, w.y0 + c0 + c * 32, w.g, w.x0 + arow + q * 32);
+          ptx::bulk_commit_group();
+        }
+      }
+    };
     int itq = 0;  // stage counter of the fused activation quantisation
     if constexpr (FUSED) {
       // Scale-atom rows past the token tile (BN < 128) never change: 127.
@@ -1221,6 +1074,149 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
       }
       ptx::griddep_wait();  // positions (and x, via TMA) come from preceding kernels
     }
+    if constexpr (QUANT) {
+      // Quantising pair form: between accumulator drains (which go first)
+      // this warp quantises its activation slices; every wait is a
+      // non-blocking test, bounded in wall time while nothing is ready.
+      // This warp quantises slice qw (rows t0 + 16 qw + [0, 16)) of every job
+      // of its CTA, in job order, from its own slot: it copies the next
+      // job's slice into the slot with TMA as soon as the current one is
+      // read, and prefetches the slice kQPrefetch jobs ahead into L2.
+      // Publication: every kQPublish slices (each of the first few, when
+      // nothing else is ready, and the last) the warp makes its earlier
+      // slices' writes visible at gpu scope and raises their jobs' counters,
+      // just before the current slice's stores, so that the fence finds the
+      // earlier stores done.
+      const int qw = warp - kEpiWarp0;
+      uint8_t* qslot = smem + C::OFF_QX + qw * kQSliceBytes;
+      uint64_t* qbar = &qfull[qw];
+      QJob j;
+      bool have = qjob_first(p, u_first, u_step, (int)rank, j);
+      int k = 0, npend = 0;  // slices copied into the slot; counters not yet raised
+      int pend[kQPublish];
+      auto pos_of = [&](const QJob& jj) -> int64_t {
+        const int t = jj.t0 + kQRows * qw + (lane & 15);
+        return (p.R > 0 && t < p.T) ? __ldg(p.pos + t) : 0;
+      };
+      auto load_slice = [&](const QJob& jj) {
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(qbar, kQSliceBytes);
+          ptx::tma_load_3d(qslot, &tm_xq, qbar, jj.kg * 128, jj.g, jj.t0 + kQRows * qw);
+        }
+      };
+      QJob jp = j;  // L2 prefetch cursor
+      bool pmore = have;
+      auto prefetch_next = [&]() {
+        if (pmore) pmore = qjob_next(p, u_step, (int)rank, jp);
+        if (pmore && lane == 0) ptx::tma_prefetch_3d(&tm_xq, jp.kg * 128, jp.g, jp.t0 + kQRows * qw);
+      };
+      auto q_publish = [&]() {
+        // The codes and atom words are read by other CTAs through TMA.
+        ptx::fence_proxy_async_global();
+        ptx::fence_acq_rel_gpu();
+        __syncwarp();
+        if (lane < npend) {
+          int f = pend[0];
+#pragma unroll
+          for (int i = 1; i < kQPublish; ++i)
+            if (lane == i) f = pend[i];
+          ptx::red_add_relaxed_gpu(p.qflags + f, 1u);
+        }
+        npend = 0;
+      };
+      ptx::griddep_wait();  // x, the positions and the cleared counters come from preceding work
+      int64_t pl = 0;
+      if (have) {
+        pl = pos_of(j);
+        load_slice(j);
+        for (int i = 0; i < kQPrefetch; ++i) prefetch_next();
+      }
+      auto q_ready = [&]() {
+        return __all_sync(0xffffffffu, ptx::mbar_test(qbar, (uint32_t)k & 1u));
+      };
+      auto q_step = [&]() {
+        const QJob jc = j;
+        const int64_t plc = pl;
+        const uint32_t badmask =
+            __ballot_sync(0xffffffffu, p.R > 0 && jc.t0 + kQRows * qw + (lane & 15) < p.T &&
+                                           (plc < 0 || plc >= p.max_pos)) & 0xFFFFu;
+        QJob jn = j;
+        const bool more = qjob_next(p, u_step, (int)rank, jn);
+        const int64_t pn = more ? pos_of(jn) : 0;
+        const bool due = npend == kQPublish || (npend > 0 && k < kQPublish);
+        // Once this warp's reads of the slot are done: copy the next slice in.
+        auto refill = [&]() {
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (more) load_slice(jn);
+          prefetch_next();
+        };
+        if (p.R > 0 && jc.kg == p.KG - 1) {
+          if (due) q_publish();
+          qslice_rope(p, jc, qw, qslot, lane, badmask, plc);
+          refill();
+        } else {
+          qslice_plain(p, jc, qw, qslot, lane, badmask, refill, [&]() {
+            if (due) q_publish();
+          });
+        }
+        if (badmask != 0 && jc.kg == 0 && lane == 0 && p.err_flag != nullptr)
+          atomicOr(p.err_flag, MXQ_DEVERR_POSITION);
+#pragma unroll
+        for (int i = 0; i < kQPublish; ++i)
+          if (i == npend) pend[i] = jc.f;
+        ++npend;
+        ++k;
+        j = jn;
+        pl = pn;
+        have = more;
+      };
+      int u = u_first;
+      uint64_t idle0 = 0;
+      bool aborted = false;
+      while (u < p.units || have) {
+        if (u < p.units &&
+            __all_sync(0xffffffffu, ptx::mbar_test(acc_full, (uint32_t)(ti & 1)))) {
+          ptx::tc_fence_after();
+          pair_drain(decode_unit<SWAP, BN>(p, u));
+          ++ti;
+          u += u_step;
+          idle0 = 0;
+          continue;
+        }
+        if (have && q_ready()) {
+          q_step();
+          idle0 = 0;
+          continue;
+        }
+        if (npend > 0) {  // nothing ready: publish what is pending now
+          q_publish();
+          continue;
+        }
+        int give_up = 0;  // 1: another role aborted, 2: nothing became ready in time
+        if (lane == 0) {
+          const uint64_t now = ptx::globaltimer();
+          if (*abort_flag)
+            give_up = 1;
+          else if (idle0 == 0)
+            idle0 = now;
+          else if (now - idle0 > kWaitLimitNs)
+            give_up = 2;
+        }
+        give_up = __shfl_sync(0xffffffffu, give_up, 0);
+        if (give_up) {
+          if (give_up == 2 && lane == 0) watchdog(abort_flag, kWdEpilogue);
+          aborted = true;
+          break;
+        }
+        __nanosleep(kEpiPollNs);
+      }
+      if (!aborted && npend > 0) q_publish();
+      // A copy still in flight into the slot (after an abort) lands before
+      // the CTA may retire.
+      if (have && !ptx::mbar_wait(qbar, (uint32_t)k & 1u, kWaitLimitNs) && lane == 0)
+        watchdog(abort_flag, kWdDrain);
+    } else
     for (int u = u_first; u < p.units; u += u_step) {
       const Unit w = decode_unit<SWAP, BN>(p, u);
       if constexpr (FUSED) {
@@ -1327,45 +1323,8 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
       }
       ptx::tc_fence_after();
       if constexpr (PAIR) {
-        // Drain 32 columns at a time and keep them as packed BF16 pairs (RNE,
-        // as in the other forms), so that the 13-warp CTA fits its register
-        // budget; the accumulator is released as soon as it is read.
-        uint32_t pk[C::HALF / 2];
-#pragma unroll
-        for (int c = 0; c < C::HALF / 32; ++c) {
-          uint32_t t32[32];
-          ptx::tmem_ld_32x32b_x32(trow + c * 32, t32);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) pk[c * 16 + j] = pack_bf16x2(t32[2 * j], t32[2 * j + 1]);
-        }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0)  // the accumulator may be overwritten now
-          ptx::mbar_arrive_remote(ptx::map_shared_rank(ptx::smem_u32(acc_empty), 0));
+        pair_drain(w);
         ++ti;
-        // Rows of a lane are 16 KB apart in the output, so each warp stages
-        // 32 rows x 32 columns in shared memory and one lane stores the box
-        // with TMA (full lines, no per-lane scattered stores; rows past T
-        // and columns past N are clipped by the copy).
-        const int c0 = h * C::HALF;
-        uint8_t* buf = smem + C::OFF_OUT + (warp - kEpiWarp0) * C::OUT_TILE;
-#pragma unroll
-        for (int c = 0; c < C::HALF / 32; ++c) {
-          if (lane == 0) ptx::bulk_wait_read<0>();  // the previous chunk's store has read it
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4*>(buf + lane * 64 + j * 16) =
-                make_uint4(pk[c * 16 + j * 4 + 0], pk[c * 16 + j * 4 + 1], pk[c * 16 + j * 4 + 2],
-                           pk[c * 16 + j * 4 + 3]);
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::tma_store_3d(&tm_out, buf, w.y0 + c0 + c * 32, w.g, w.x0 + arow + q * 32);
-            ptx::bulk_commit_group();
-          }
-        }
         continue;
       }
       uint32_t v[C::HALF];
