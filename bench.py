@@ -301,18 +301,16 @@ def stream_100k(mxq, device):
         pos = torch.arange(start, start + T, dtype=torch.int64, device=device)
         chunks.append((x, pos))
         start += T
-    q = torch.empty((8192, G, D), dtype=torch.uint8, device=device)
-    sc = torch.empty((8192, G, KG), dtype=torch.uint8, device=device)
     o = torch.empty((8192, G, N), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(mxq.mxq_wo_a_workspace_bytes(8192, G, D, N), dtype=torch.uint8, device=device)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(chunks) + 1)]
 
-    def run():
+    def run():  # mxq_wo_a per (chunk, layer): one launch each
         for ci, (x, pos) in enumerate(chunks):
             ev[ci].record()
             T = x.shape[0]
             for wq, wsf, _ in wsets:
-                mxq.mxq_inv_rope_group_quant(x, pos, cos, sin, R, q=q[:T], sc=sc[:T])
-                mxq.mxq_bmm_a8w8(q[:T], sc[:T], wq, wsf, out=o[:T])
+                mxq.wo_a(x, pos, cos, sin, wq, wsf, R=R, out=o[:T], ws=ws)
         ev[-1].record()
 
     run()
@@ -563,9 +561,22 @@ def main():
     q = torch.empty((T_PREFILL, G, D), dtype=torch.uint8, device=device)
     sc = torch.empty((T_PREFILL, G, KG), dtype=torch.uint8, device=device)
     out = torch.empty((T_PREFILL, G, N), dtype=torch.bfloat16, device=device)
+    wo_ws = torch.empty(mxq.mxq_wo_a_workspace_bytes(T_PREFILL, G, D, N), dtype=torch.uint8,
+                        device=device)
     stream = torch.cuda.current_stream()
 
     def step(i, evs=None):
+        # One library call: the quantising CTA-pair GEMM (one kernel, after a
+        # clear of its job counters).
+        wq, wsf, _ = wsets[i % N_WSETS]
+        if evs is not None:
+            evs[0].record(stream)
+        mxq.wo_a(x, pos, cos, sin, wq, wsf, R=R, out=out, ws=wo_ws, stream=stream)
+        if evs is not None:
+            evs[1].record(stream)
+
+    def two_kernel_step(i, evs=None):
+        # The same projection as quantiser + GEMM (two kernels), for comparison.
         wq, wsf, _ = wsets[i % N_WSETS]
         if evs is not None:
             evs[0].record(stream)
@@ -583,11 +594,10 @@ def main():
 
     clocks = ClockSampler(local_rank)
     clocks.start()
-    # Every 10th step is bracketed with CUDA events for the per-kernel times;
-    # the others run with nothing between the two launches, as in use, so
-    # that the GEMM can launch early (programmatic dependent launch).
+    # Every 10th step is bracketed with CUDA events for the kernel time; the
+    # others run back to back, as in use.
     sampled = list(range(0, args.steps, 10))
-    evs = {i: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for i in sampled}
+    evs = {i: [torch.cuda.Event(enable_timing=True) for _ in range(2)] for i in sampled}
     barrier()
     torch.cuda.synchronize()
     t_host0 = time.time()
@@ -603,11 +613,30 @@ def main():
     clk = clocks.summary(t_host0, t_host1)
 
     ms_total = start.elapsed_time(end)
-    t_quant = sum(e[0].elapsed_time(e[1]) for e in evs.values()) / len(evs)
-    t_gemm = sum(e[1].elapsed_time(e[2]) for e in evs.values()) / len(evs)
+    t_fused = sum(e[0].elapsed_time(e[1]) for e in evs.values()) / len(evs)
     ms_step = ms_total / args.steps
     ms_step = max_over_ranks(ms_step, device)
     value = job_throughput(world, T_PREFILL, ms_step)
+
+    # The same projection as quantiser + GEMM (two kernels), for comparison:
+    # steps back to back for the step time, then bracketed ones for the
+    # per-kernel times and rooflines.
+    n_two = max(10, min(args.steps, 50))
+    for i in range(args.warmup):
+        two_kernel_step(i)
+    torch.cuda.synchronize()
+    a2, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a2.record(stream)
+    for i in range(n_two):
+        two_kernel_step(i)
+    b2.record(stream)
+    evs2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(10)]
+    for i, e in enumerate(evs2):
+        two_kernel_step(i, e)
+    torch.cuda.synchronize()
+    ms_two = a2.elapsed_time(b2) / n_two
+    t_quant = sum(e[0].elapsed_time(e[1]) for e in evs2) / len(evs2)
+    t_gemm = sum(e[1].elapsed_time(e[2]) for e in evs2) / len(evs2)
 
     # End to end through the public API: pinned host x -> device, wo_a, output
     # -> host, every step.  The steps are pipelined on three streams (copy
@@ -622,8 +651,6 @@ def main():
     pos_dev = [torch.empty_like(pos) for _ in range(2)]
     out_dev = [torch.empty((T_PREFILL, G, N), dtype=torch.bfloat16, device=device)
                for _ in range(2)]
-    wo_ws = torch.empty(mxq.mxq_wo_a_workspace_bytes(T_PREFILL, G, D, N), dtype=torch.uint8,
-                        device=device)
     e2e_steps = max(3, min(args.steps, 20))
     s_in, s_comp, s_out = (torch.cuda.Stream(device=device) for _ in range(3))
 
@@ -678,9 +705,9 @@ def main():
     del x_host, out_host
 
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
+    fused_tflops = gemm_flops(T_PREFILL) / (t_fused * 1e-3) / 1e12
     gemm_tflops = gemm_flops(T_PREFILL) / (t_gemm * 1e-3) / 1e12
     quant_gbs = quant_bytes(T_PREFILL) / (t_quant * 1e-3) / 1e9
-    traffic = measured_traffic("bmm_a8w8_prefill_8k")
 
     sec = {}
     if not args.no_secondary and rank == 0:
@@ -696,18 +723,28 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
             "data": "synthetic",
             "config": prefill_config(world),
-            "gpu_launches": 2 * args.steps,
-            "breakdown_ms": {"quant": round(t_quant, 5), "gemm": round(t_gemm, 5)},
-            "roofline": {"bound": "tensor", "kernel": "bmm_a8w8 (prefill)",
-                         "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
-                         "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
-                         "traffic": traffic,
+            "gpu_launches": args.steps,
+            "breakdown_ms": {"wo_a_one_launch": round(t_fused, 5)},
+            "roofline": {"bound": "tensor",
+                         "kernel": "bmm_a8w8 quantising CTA-pair form (the whole wo_a chunk, one launch)",
+                         "achieved": round(fused_tflops, 1), "peak": round(fp8_peak, 1),
+                         "unit": "TFLOP/s", "frac": round(fused_tflops / fp8_peak, 4),
+                         "traffic": measured_traffic("wo_a_prefill_8k"),
                          "peak_source": f"{peaks['source']}: 2 x sustained bf16 "
                                         f"{peaks['bf16_tflops_sustained']} TFLOP/s (fp8/bf16 nominal 4.5/2.25)"},
-            "quantiser_roofline": {"bound": "hbm", "achieved": round(quant_gbs, 1),
-                                   "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                   "frac": round(quant_gbs / peaks["hbm_gbs"], 4),
-                                   "traffic": measured_traffic("inv_rope_group_quant_prefill_8k")},
+            "two_kernel": {
+                "what": "the same chunk as quantiser + GEMM (two launches)",
+                "ms_per_step": round(ms_two, 5),
+                "value": round(T_PREFILL / (ms_two * 1e-3), 1),
+                "breakdown_ms": {"quant": round(t_quant, 5), "gemm": round(t_gemm, 5)},
+                "gemm_roofline": {"bound": "tensor", "achieved": round(gemm_tflops, 1),
+                                  "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                                  "frac": round(gemm_tflops / fp8_peak, 4),
+                                  "traffic": measured_traffic("bmm_a8w8_prefill_8k")},
+                "quantiser_roofline": {"bound": "hbm", "achieved": round(quant_gbs, 1),
+                                       "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                       "frac": round(quant_gbs / peaks["hbm_gbs"], 4),
+                                       "traffic": measured_traffic("inv_rope_group_quant_prefill_8k")}},
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                     "schedule": "mxq_wo_a per step; copy-in, compute and copy-out on three "

@@ -76,6 +76,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <type_traits>
 #include <utility>
 #include <mutex>
 
@@ -462,6 +463,20 @@ __device__ __forceinline__ void qslice_plain(const BmmArgs& p, const QJob& j, in
   }
 }
 
+// Tensor maps only the quantising form takes (the activation scale atoms it
+// writes and its BF16 input); the other forms take an empty parameter, so
+// that their launches copy no more parameter bytes than they use.
+struct QuantMaps {
+  CUtensorMap asf, xq;
+};
+struct NoMaps {};
+template <bool QUANT>
+using QuantMapsT = typename std::conditional<QUANT, QuantMaps, NoMaps>::type;
+__device__ __forceinline__ const CUtensorMap* map_asf(const QuantMaps& m) { return &m.asf; }
+__device__ __forceinline__ const CUtensorMap* map_xq(const QuantMaps& m) { return &m.xq; }
+__device__ __forceinline__ const CUtensorMap* map_asf(const NoMaps&) { return nullptr; }
+__device__ __forceinline__ const CUtensorMap* map_xq(const NoMaps&) { return nullptr; }
+
 template <bool SWAP, bool FUSED, int BN, int NSTAGE, bool PAIR, bool QUANT>
 __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::THREADS),
                                   (Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::CTAS_PER_SM))
@@ -469,8 +484,7 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
                     const __grid_constant__ CUtensorMap tm_w,
                     const __grid_constant__ CUtensorMap tm_wsf,
                     const __grid_constant__ CUtensorMap tm_out,
-                    const __grid_constant__ CUtensorMap tm_asf,
-                    const __grid_constant__ CUtensorMap tm_xq, const BmmArgs p) {
+                    const __grid_constant__ QuantMapsT<QUANT> qmaps, const BmmArgs p) {
   using C = Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -533,8 +547,8 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
     ptx::prefetch_tmap(&tm_w);
     if (PAIR) ptx::prefetch_tmap(&tm_wsf);
     if (QUANT) {
-      ptx::prefetch_tmap(&tm_asf);
-      ptx::prefetch_tmap(&tm_xq);
+      ptx::prefetch_tmap(map_asf(qmaps));
+      ptx::prefetch_tmap(map_xq(qmaps));
     }
   }
   if (warp == 1) {
@@ -766,7 +780,7 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
           ptx::tma_load_3d_pair(smem + C::OFF_X + s * C::X_TILE, &tm_act, bar, (w.kg_begin + kk) * 128,
                                 w.g, w.x0 + arow);
         } else if (lane == 1) {
-          ptx::tma_load_2d_pair(smem + C::OFF_SFX + s * C::SFX_BYTES, &tm_asf, bar, 0,
+          ptx::tma_load_2d_pair(smem + C::OFF_SFX + s * C::SFX_BYTES, map_asf(qmaps), bar, 0,
                                 2 * (fbase + kk));
         }
         __syncwarp();
@@ -1020,48 +1034,6 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + h * C::HALF;
     float* red = reinterpret_cast<float*>(smem + C::OFF_RED);  // split-K receive buffer
     int ti = 0;
-    // Pair form: drains this warp's quarter of the unit's accumulator (after
-    // its acc_full phase) and stores it.
-    auto pair_drain = [&](const Unit& w) {
-      // Drain 32 columns at a time and keep them as packed BF16 pairs (RNE,
-      // as in the other forms), so that the 13-warp CTA fits its register
-      // budget; the accumulator is released as soon as it is read.
-      uint32_t pk[C::HALF / 2];
-#pragma unroll
-      for (int c = 0; c < C::HALF / 32; ++c) {
-        uint32_t t32[32];
-        ptx::tmem_ld_32x32b_x32(trow + c * 32, t32);
-        ptx::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) pk[c * 16 + j] = pack_bf16x2(t32[2 * j], t32[2 * j + 1]);
-      }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0)  // the accumulator may be overwritten now
-        ptx::mbar_arrive_remote(ptx::map_shared_rank(ptx::smem_u32(acc_empty), 0));
-      // Rows of a lane are 16 KB apart in the output, so each warp stages
-      // 32 rows x 32 columns in shared memory and one lane stores the box
-      // with TMA (full lines, no per-lane scattered stores; rows past T
-      // and columns past N are clipped by the copy).
-      const int c0 = h * C::HALF;
-      uint8_t* buf = smem + C::OFF_OUT + (warp - kEpiWarp0) * C::OUT_TILE;
-#pragma unroll
-      for (int c = 0; c < C::HALF / 32; ++c) {
-        if (lane == 0) ptx::bulk_wait_read<0>();  // the previous chunk's store has read it
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4*>(buf + lane * 64 + j * 16) =
-              make_uint4(pk[c * 16 + j * 4 + 0], pk[c * 16 + j * 4 + 1], pk[c * 16 + j * 4 + 2],
-                         pk[c * 16 + j * 4 + 3]);
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          ptx::tma_store_3d(&tm_out, buf, w.y0 + c0 + c * 32, w.g, w.x0 + arow + q * 32);
-          ptx::bulk_commit_group();
-        }
-      }
-    };
     int itq = 0;  // stage counter of the fused activation quantisation
     if constexpr (FUSED) {
       // Scale-atom rows past the token tile (BN < 128) never change: 127.
@@ -1088,6 +1060,51 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
       // just before the current slice's stores, so that the fence finds the
       // earlier stores done.
       const int qw = warp - kEpiWarp0;
+      // Drains this warp's quarter of the unit's accumulator (after its
+      // acc_full phase) and stores it, as the plain pair form's loop below
+      // does.  (The two copies are kept apart: a drain shared by every form's
+      // epilogue measured 0.8 us per layer slower in the few-token forms,
+      // which never drain this way.)
+      auto pair_drain = [&](const Unit& w) {
+        // Drain 32 columns at a time and keep them as packed BF16 pairs (RNE,
+        // as in the other forms), so that the 13-warp CTA fits its register
+        // budget; the accumulator is released as soon as it is read.
+        uint32_t pk[C::HALF / 2];
+  #pragma unroll
+        for (int c = 0; c < C::HALF / 32; ++c) {
+          uint32_t t32[32];
+          ptx::tmem_ld_32x32b_x32(trow + c * 32, t32);
+          ptx::tmem_ld_wait();
+  #pragma unroll
+          for (int j = 0; j < 16; ++j) pk[c * 16 + j] = pack_bf16x2(t32[2 * j], t32[2 * j + 1]);
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0)  // the accumulator may be overwritten now
+          ptx::mbar_arrive_remote(ptx::map_shared_rank(ptx::smem_u32(acc_empty), 0));
+        // Rows of a lane are 16 KB apart in the output, so each warp stages
+        // 32 rows x 32 columns in shared memory and one lane stores the box
+        // with TMA (full lines, no per-lane scattered stores; rows past T
+        // and columns past N are clipped by the copy).
+        const int c0 = h * C::HALF;
+        uint8_t* buf = smem + C::OFF_OUT + (warp - kEpiWarp0) * C::OUT_TILE;
+  #pragma unroll
+        for (int c = 0; c < C::HALF / 32; ++c) {
+          if (lane == 0) ptx::bulk_wait_read<0>();  // the previous chunk's store has read it
+          __syncwarp();
+  #pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(buf + lane * 64 + j * 16) =
+                make_uint4(pk[c * 16 + j * 4 + 0], pk[c * 16 + j * 4 + 1], pk[c * 16 + j * 4 + 2],
+                           pk[c * 16 + j * 4 + 3]);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(&tm_out, buf, w.y0 + c0 + c * 32, w.g, w.x0 + arow + q * 32);
+            ptx::bulk_commit_group();
+          }
+        }
+      };
       uint8_t* qslot = smem + C::OFF_QX + qw * kQSliceBytes;
       uint64_t* qbar = &qfull[qw];
       QJob j;
@@ -1101,14 +1118,14 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
       auto load_slice = [&](const QJob& jj) {
         if (lane == 0) {
           ptx::mbar_arrive_expect_tx(qbar, kQSliceBytes);
-          ptx::tma_load_3d(qslot, &tm_xq, qbar, jj.kg * 128, jj.g, jj.t0 + kQRows * qw);
+          ptx::tma_load_3d(qslot, map_xq(qmaps), qbar, jj.kg * 128, jj.g, jj.t0 + kQRows * qw);
         }
       };
       QJob jp = j;  // L2 prefetch cursor
       bool pmore = have;
       auto prefetch_next = [&]() {
         if (pmore) pmore = qjob_next(p, u_step, (int)rank, jp);
-        if (pmore && lane == 0) ptx::tma_prefetch_3d(&tm_xq, jp.kg * 128, jp.g, jp.t0 + kQRows * qw);
+        if (pmore && lane == 0) ptx::tma_prefetch_3d(map_xq(qmaps), jp.kg * 128, jp.g, jp.t0 + kQRows * qw);
       };
       auto q_publish = [&]() {
         // The codes and atom words are read by other CTAs through TMA.
@@ -1323,7 +1340,44 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
       }
       ptx::tc_fence_after();
       if constexpr (PAIR) {
-        pair_drain(w);
+        // Drain 32 columns at a time and keep them as packed BF16 pairs (RNE,
+        // as in the other forms), so that the 13-warp CTA fits its register
+        // budget; the accumulator is released as soon as it is read.
+        uint32_t pk[C::HALF / 2];
+  #pragma unroll
+        for (int c = 0; c < C::HALF / 32; ++c) {
+          uint32_t t32[32];
+          ptx::tmem_ld_32x32b_x32(trow + c * 32, t32);
+          ptx::tmem_ld_wait();
+  #pragma unroll
+          for (int j = 0; j < 16; ++j) pk[c * 16 + j] = pack_bf16x2(t32[2 * j], t32[2 * j + 1]);
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0)  // the accumulator may be overwritten now
+          ptx::mbar_arrive_remote(ptx::map_shared_rank(ptx::smem_u32(acc_empty), 0));
+        // Rows of a lane are 16 KB apart in the output, so each warp stages
+        // 32 rows x 32 columns in shared memory and one lane stores the box
+        // with TMA (full lines, no per-lane scattered stores; rows past T
+        // and columns past N are clipped by the copy).
+        const int c0 = h * C::HALF;
+        uint8_t* buf = smem + C::OFF_OUT + (warp - kEpiWarp0) * C::OUT_TILE;
+  #pragma unroll
+        for (int c = 0; c < C::HALF / 32; ++c) {
+          if (lane == 0) ptx::bulk_wait_read<0>();  // the previous chunk's store has read it
+          __syncwarp();
+  #pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(buf + lane * 64 + j * 16) =
+                make_uint4(pk[c * 16 + j * 4 + 0], pk[c * 16 + j * 4 + 1], pk[c * 16 + j * 4 + 2],
+                           pk[c * 16 + j * 4 + 3]);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(&tm_out, buf, w.y0 + c0 + c * 32, w.g, w.x0 + arow + q * 32);
+            ptx::bulk_commit_group();
+          }
+        }
         ++ti;
         continue;
       }
@@ -1604,7 +1658,12 @@ cudaError_t launch_cfg(const void* a, const uint8_t* w, BmmArgs args, int num_sm
     grid = args.units < slots ? args.units : slots;
   }
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, tm_act, tm_w, tm_wsf, tm_out, tm_asf, tm_xq, args);
+  QuantMapsT<QUANT> qmaps{};
+  if constexpr (QUANT) {
+    qmaps.asf = tm_asf;
+    qmaps.xq = tm_xq;
+  }
+  return cudaLaunchKernelEx(&cfg, kern, tm_act, tm_w, tm_wsf, tm_out, qmaps, args);
 }
 
 }  // namespace
