@@ -117,7 +117,7 @@ constexpr uint32_t kFlagPollNs = 128;
 constexpr uint32_t kEpiPollNs = 32;
 // Each quantising warp prefetches its slice of the job this many jobs ahead
 // into L2 (its shared-memory copies then wait on L2, not DRAM).
-constexpr int kQPrefetch = 4;
+constexpr int kQPrefetch = 2;
 // Publications are batched (and made at once whenever the warp has nothing
 // else ready): the gpu-scope fence waits for every store the warp still has
 // in flight.
