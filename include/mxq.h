@@ -175,8 +175,10 @@ int mxq_linear(const void* x_bf16, const uint8_t* w_e4m3, const uint8_t* w_sf_pr
                void* out_bf16, int64_t M, int32_t N, int32_t K, void* ws, size_t ws_bytes,
                mxq_stream_t stream);
 
-/* Workspace bytes mxq_wo_a needs: 0 for T <= 32, else T*G*D code bytes and
- * T*G*ceil(D/128) scale bytes (each rounded up to 256). */
+/* Workspace bytes mxq_wo_a needs: 0 for T <= 32; for 32 < T <= 128, T*G*D
+ * code bytes and T*G*ceil(D/128) scale bytes; for T > 128, T*G*D code
+ * bytes, G*MB*ceil(D/128)*512 scale-atom bytes and G*MB*ceil(D/128)*4
+ * job-counter bytes with MB = 2*ceil(T/256) (each region rounded up to 256). */
 size_t mxq_wo_a_workspace_bytes(int64_t T, int32_t G, int32_t D, int32_t N);
 
 /*
@@ -187,9 +189,14 @@ size_t mxq_wo_a_workspace_bytes(int64_t T, int32_t G, int32_t D, int32_t N);
  *
  * For T <= 32 tokens (decode) it is ONE launch: the GEMM reads the BF16 x
  * and quantises each tile itself, so neither the codes nor a second launch
- * cost anything (this goes beyond the pages' two-kernel design).  For larger
- * T the codes go through `ws` (mxq_wo_a_workspace_bytes) and two kernels run.
- * err_flag as in mxq_inv_rope_group_quant.  T == 0 is a no-op.
+ * cost anything (this goes beyond the pages' two-kernel design).  For
+ * 32 < T <= 128 the codes go through `ws` and two kernels run.  For T > 128
+ * (prefill) it is again ONE launch: warps of the CTA-pair GEMM quantise x
+ * into `ws` (codes, scale atoms, and per-job counters that the call clears
+ * first) while the MMA pipeline consumes what is ready.  `ws` holds
+ * mxq_wo_a_workspace_bytes(T, G, D, N) bytes, 16-byte aligned; calls that
+ * may run at the same time need distinct workspaces.  err_flag as in
+ * mxq_inv_rope_group_quant.  T == 0 is a no-op.
  */
 int mxq_wo_a(const void* x_bf16, const int64_t* pos, const void* cos_bf16, const void* sin_bf16,
              int64_t cs_ld, int64_t max_pos, const uint8_t* w_e4m3, const uint8_t* w_sf_prepared,
