@@ -156,9 +156,10 @@ int mxq_bmm_a8w8(const uint8_t* a_e4m3, const uint8_t* a_e8m0, const uint8_t* w_
                  const uint8_t* w_sf_prepared, void* out_bf16, int64_t T, int32_t G, int32_t N,
                  int32_t K, void* ws, size_t ws_bytes, mxq_stream_t stream);
 
-/* Workspace bytes mxq_linear needs: 0 for M <= 32 (one fused launch),
- * otherwise the quantised activation codes and scales plus the GEMM
- * workspace. */
+/* Workspace bytes mxq_linear needs: 0 for M <= 32 (one fused launch); for
+ * 32 < M <= 128 the quantised activation codes and scales plus the GEMM
+ * workspace; above, mxq_wo_a_workspace_bytes(M, 1, K, N) (one launch that
+ * quantises inside the GEMM). */
 size_t mxq_linear_workspace_bytes(int64_t M, int32_t N, int32_t K);
 
 /*
@@ -167,8 +168,8 @@ size_t mxq_linear_workspace_bytes(int64_t M, int32_t N, int32_t K);
  * (dequantise-once page, Purpose: K = 576 at TP4, 288 at TP8).  x is BF16;
  * it is quantised per row in groups of 128 exactly as
  * mxq_inv_rope_group_quant with R = 0 and multiplied as mxq_bmm_a8w8 with
- * G = 1: for M <= 32 in one launch that quantises inside the GEMM, else
- * through the workspace.  w_sf_prepared from
+ * G = 1: for M <= 32 and for M > 128 in one launch that quantises inside
+ * the GEMM, in between through the workspace.  w_sf_prepared from
  * mxq_prepare_weight_scales(.., B=1, N, K).  M == 0 is a no-op.
  */
 int mxq_linear(const void* x_bf16, const uint8_t* w_e4m3, const uint8_t* w_sf_prepared,

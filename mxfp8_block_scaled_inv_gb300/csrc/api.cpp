@@ -201,6 +201,7 @@ int mxq_bmm_a8w8(const uint8_t* a_e4m3, const uint8_t* a_e8m0, const uint8_t* w_
 size_t mxq_linear_workspace_bytes(int64_t M, int32_t N, int32_t K) {
   if (M < 0 || N < 1 || K < 1) return 0;
   if (M <= mxq::kFusedMaxTokens) return 0;  // one fused launch, no scratch
+  if (M >= mxq::kPairMinTokens) return mxq::woa_prefill_layout(M, 1, K).total;
   return round256((size_t)M * K) + round256((size_t)M * kgroups(K)) +
          round256(mxq_bmm_workspace_bytes(M, 1, N, K));
 }
@@ -232,6 +233,19 @@ int mxq_linear(const void* x_bf16, const uint8_t* w_e4m3, const uint8_t* w_sf_pr
   if (!ws || ws_bytes < need)
     return fail(MXQ_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, ws_bytes);
   if (!aligned16(ws)) return fail(MXQ_ERR_ALIGN, "workspace must be 16-byte aligned");
+  if (M >= mxq::kPairMinTokens) {
+    // Many rows: one launch of the CTA-pair GEMM whose warps quantise x.
+    if (M * kgroups(K) >= (int64_t)1 << 31)
+      return fail(MXQ_ERR_UNSUPPORTED, "M*ceil(K/128) must be < 2^31");
+    int sms = 0;
+    if (int st = device_check(&sms)) return st;
+    const char* why = nullptr;
+    cudaError_t e = mxq::launch_wo_a_prefill(x_bf16, nullptr, nullptr, nullptr, 0, 0, 0, w_e4m3,
+                                             w_sf_prepared, out_bf16, M, 1, N, K, nullptr, ws, sms,
+                                             static_cast<cudaStream_t>(stream), &why);
+    if (e != cudaSuccess && why) return fail(MXQ_ERR_CUDA, "linear: %s", why);
+    return cuda_status(e, "linear (quantising pair form) launch");
+  }
   uint8_t* codes = static_cast<uint8_t*>(ws);
   uint8_t* scales = codes + round256((size_t)M * K);
   uint8_t* gemm_ws = scales + round256((size_t)M * kgroups(K));

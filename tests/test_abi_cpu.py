@@ -106,6 +106,8 @@ def test_linear_argument_errors(L):
     assert L.mxq_linear_workspace_bytes(8, 5120, 576) == 0  # <= 32 rows: one fused launch
     need = L.mxq_linear_workspace_bytes(100, 5120, 576)
     assert need == 100 * 576 + 512  # codes (57600 B, 256-aligned) + 100*5 scale bytes -> 512
+    # Above 128 rows: one launch, the workspace of mxq_wo_a with G = 1.
+    assert L.mxq_linear_workspace_bytes(300, 5120, 576) == L.mxq_wo_a_workspace_bytes(300, 1, 576, 5120)
     assert L.mxq_linear(P, P, P, P, 100, 5120, 576, None, 0, None) == 6
     assert L.mxq_linear(P, P, P, P, 100, 5120, 576, P, need - 1, None) == 6
     assert L.mxq_linear(None, P, P, P, 8, 5120, 576, P, need, None) == 1

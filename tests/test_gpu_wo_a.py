@@ -1,6 +1,7 @@
 """GPU parity of mxq_wo_a, the whole wo_a projection in one call (one fused
-launch for T <= 32, quantiser + GEMM through a workspace above), against the
-oracle: inverse RoPE + group quantisation, then the block-scaled GEMM."""
+launch for T <= 32, quantiser + GEMM through a workspace for 32 < T <= 128,
+one launch of the quantising CTA-pair GEMM above), against the oracle:
+inverse RoPE + group quantisation, then the block-scaled GEMM."""
 
 import numpy as np
 import pytest
@@ -54,8 +55,9 @@ def test_ragged_tokens_and_rope_widths(mxq, T, R):
     check_gemm(out, *O.bmm_a8w8_ref(a, sa, w, sw), f"T={T} R={R}")
 
 
-@pytest.mark.parametrize("T", [33, 65, 100, 300])
-def test_larger_token_counts_use_two_kernels(mxq, T):
+@pytest.mark.parametrize("T", [33, 65, 100, 128, 129, 300])
+def test_larger_token_counts(mxq, T):
+    """Both sides of each boundary between the forms (32/33, 128/129)."""
     x, pos, cos, sin = wo_a_inputs(T, 2, 1024, 256, 64, seed=1500 + T, max_pos=4096)
     w, sw = oracle_weights(2, 256, 1024, seed=1501)
     out, _ = run(mxq, x, pos, cos, sin, w, sw, 64)
