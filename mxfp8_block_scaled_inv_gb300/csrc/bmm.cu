@@ -54,20 +54,20 @@
 //           One launch then does the whole wo_a (or MXFP8 linear) step, with
 //           no round trip of the codes through HBM.
 //   pair + quantise (many tokens, wo_a): the pair form, reading the BF16
-//           activation.  Four more warps of each CTA (warp 2 and warps 13-15)
+//           activation.  Between accumulator drains the 8 epilogue warps
 //           quantise the CTA's own 128 token rows (inverse RoPE on the last
-//           group, group scale, E4M3 codes) into a workspace, ahead of the
-//           MMAs and independently of them: the codes go to global memory in
-//           the [T][G][K] layout and the scale bytes as ready-made scale atoms,
-//           and a per-(128 rows, K group) counter in global memory is raised
-//           once the writes are visible.  The units of one 256-token block
-//           are taken by consecutive pairs, and the pair with weight tile yt
-//           quantises the K groups kg = yt (mod weight tiles) of the block, so
-//           the quantisation is spread over every SM and done once.  The
-//           activation producer polls the counters and TMA-loads the codes
-//           and atoms as soon as they are published.  The quantising warps
-//           never wait on anything, so the counters always complete (every
-//           CTA of the persistent grid is resident).
+//           group, group scale, E4M3 codes) into a workspace, independently
+//           of the MMAs: the codes go to global memory in the [T][G][K]
+//           layout and the scale bytes as ready-made scale atoms, and a
+//           per-(128 rows, K group) counter in global memory is raised once
+//           the writes are visible.  The units of one 256-token block are
+//           taken by consecutive pairs, and the y_tiles pairs that share it
+//           split its K groups, so the quantisation is spread over every SM
+//           and done once.  The activation producer reads the counters and
+//           TMA-loads the codes and atoms as soon as they are published.  The
+//           quantising work waits only for its own copies, so the counters
+//           always complete (every CTA of the persistent grid is resident).
+//           (warp 2, the scale loader in the other pair form, is idle.)
 // Every wait is bounded in wall time; on expiry the kernel sets a watchdog
 // bit, stops issuing, drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -213,8 +213,6 @@ struct Cfg {
   // The pair form adds a gate warp that does the MMA warp's barrier waits:
   // the tensor pipe's instruction queue is shallow, so any wait in the
   // issuing warp between stages leaves the pipe idle.
-  // (In the quantising pair form warp 2, the scale loader otherwise, loads
-  // the activation slices.)
   static constexpr int THREADS = (FUSED ? 11 : (PAIR ? 13 : 12)) * 32;
   // Instruction descriptor, kind::mxf8f6f4 with block scaling: E4M3 A and
   // B (format 0), both K-major, N >> 3 at bits 17-22, UE8M0 scale type at
@@ -273,11 +271,9 @@ __device__ __forceinline__ Unit decode_unit(const BmmArgs& p, int u) {
 
 // ------------------------------------------- in-kernel activation quantisation
 // A job = one K group kg of one 128-token block of one group g, done by the
-// CTA that owns the block as kQSlices slices of kQRows rows.  The quantising
-// producer (warp 2) TMA-loads each slice's BF16 values into a slot of the
-// ring of the warp that will quantise it; that warp quantises the slice into
-// global memory and raises the job's counter by one, so a finished job's
-// counter reads kQSlices.
+// CTA that owns the block as kQSlices slices of kQRows rows, slice w by
+// epilogue warp w from its own shared-memory slot; each slice raises the
+// job's counter by one, so a finished job's counter reads kQSlices.
 struct QJob {
   int u, jj;  // unit and job index within the unit
   int g, kg;  // group and K group
