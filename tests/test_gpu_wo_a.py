@@ -214,3 +214,28 @@ def test_pair_quant_deterministic_and_graph_replay(mxq):
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(out, o2)
+
+
+def test_pair_quant_repeated_runs_match_two_kernels(mxq):
+    """Production G, D, N at 2048 tokens, 20 calls on one workspace: every
+    output bit-identical to quantiser + GEMM (a missing ordering between the
+    quantising warps and the consuming CTAs would show as a sporadic
+    mismatch), and the first also against the oracle on sampled tokens."""
+    T, G, D, N = 2048, 8, 4096, 1024
+    x, pos, cos, sin = wo_a_inputs(T, G, D, N, 64, seed=2200, pos_mode="arange",
+                                   outlier_frac=0.01)
+    w, sw = oracle_weights(G, N, D, seed=3)
+    xd, pd, cd, sd, wd, swd = to_dev(x, pos, cos, sin, w, sw)
+    wsf = mxq.mxq_prepare_weight_scales(swd, D)
+    q, sc = mxq.mxq_inv_rope_group_quant(xd, pd, cd, sd, 64)
+    ref = mxq.mxq_bmm_a8w8(q, sc, wd, wsf)
+    ws = torch.empty(mxq.mxq_wo_a_workspace_bytes(T, G, D, N), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(ref)
+    for i in range(20):
+        mxq.mxq_wo_a(xd, pd, cd, sd, wd, wsf, R=64, out=out, ws=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), f"call {i} differs from quantiser + GEMM"
+        if i == 0:
+            idx = np.array([0, 127, 128, 1000, 2047])
+            a, sa = oracle_quant(x[idx], pos[idx], cos, sin, 64)
+            check_gemm(out[idx], *O.bmm_a8w8_ref(a, sa, w, sw), "sampled")
