@@ -366,25 +366,46 @@ def _oracle_weights():
     return _cache["w"]
 
 
-def cpu_baseline(budget_s=12.0):
-    """Oracle throughput on the host cores, single-threaded, on bounded samples."""
-    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    code = ("import sys,json,time; sys.path.insert(0, %r); import bench\n"
+def _oracle_subprocess(code, threads):
+    """Runs oracle timing code in a fresh interpreter whose BLAS and OpenMP use
+    exactly `threads` threads (the thread count must be fixed before numpy
+    loads); returns its last output line as JSON, or None."""
+    n = str(threads)
+    env = dict(os.environ, OPENBLAS_NUM_THREADS=n, OMP_NUM_THREADS=n, MKL_NUM_THREADS=n)
+    r = subprocess.run([sys.executable, "-c", code], env=env, stdout=subprocess.PIPE,
+                       stderr=subprocess.PIPE, text=True, timeout=900)
+    if r.returncode != 0:
+        return None
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def _oracle_budget_code(budget_s):
+    return ("import sys,json,time; sys.path.insert(0, %r); import bench\n"
             "bench._oracle_weights(); bench._oracle_tables()\n"
             "tok, el, i = 0, 0.0, 0\n"
             "while el < %f:\n"
             "    el += bench.oracle_sample_run(16, 100 + i); tok += 16; i += 1\n"
             "print(json.dumps({'tokens': tok, 'seconds': el}))\n") % (ROOT, budget_s)
-    r = subprocess.run([sys.executable, "-c", code], env=env, stdout=subprocess.PIPE,
-                       stderr=subprocess.PIPE, text=True, timeout=600)
-    if r.returncode != 0:
-        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
-                "sample": "failed: " + r.stderr.strip().splitlines()[-1] if r.stderr else "failed"}
-    d = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": round(d["tokens"] / d["seconds"], 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+
+
+def cpu_baseline(budget_s=12.0):
+    """Oracle throughput on the host cores on bounded samples: one thread (the
+    reported value), and every core (BLAS threads = the core count) beside it."""
+    d = _oracle_subprocess(_oracle_budget_code(budget_s), 1)
+    if d is None:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": "failed"}
+    line = {"value": round(d["tokens"] / d["seconds"], 3), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{d['tokens']} tokens of the 8K chunk in batches of 16 (x [16,8,4096] -> "
                       f"quantiser + fp64 GEMM against W [8,1024,4096]), {d['seconds']:.1f} s, "
                       f"one thread"}
+    ncores = os.cpu_count() or 1
+    da = _oracle_subprocess(_oracle_budget_code(budget_s * 0.5), ncores)
+    if da is not None:
+        line["all_cores"] = {"value": round(da["tokens"] / da["seconds"], 3), "unit": UNIT,
+                             "cores": ncores,
+                             "sample": f"{da['tokens']} tokens, {da['seconds']:.1f} s, BLAS on "
+                                       f"{ncores} threads (the quantiser part is single-threaded numpy)"}
+    return line
 
 
 # ---------------------------------------------------------- multi-rank glue
@@ -426,14 +447,20 @@ def prefill_config(world):
 def run_reference(args, rank):
     if rank != 0:
         return
-    _oracle_weights()
-    _oracle_tables()
     per_step = 16
-    for i in range(args.warmup):
-        oracle_sample_run(per_step, 10 + i)
-    el = 0.0
-    for i in range(args.steps):
-        el += oracle_sample_run(per_step, 1000 + i)
+    # The oracle runs in a fresh interpreter pinned to one thread (this
+    # process's numpy has already chosen its BLAS thread count).
+    code = ("import sys,json; sys.path.insert(0, %r); import bench\n"
+            "bench._oracle_weights(); bench._oracle_tables()\n"
+            "for i in range(%d): bench.oracle_sample_run(%d, 10 + i)\n"
+            "el = sum(bench.oracle_sample_run(%d, 1000 + i) for i in range(%d))\n"
+            "print(json.dumps({'seconds': el}))\n") % (ROOT, args.warmup, per_step, per_step,
+                                                        args.steps)
+    d = _oracle_subprocess(code, 1)
+    if d is None:
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle run failed"}), flush=True)
+        return
+    el = d["seconds"]
     value = per_step * args.steps / el
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
