@@ -39,8 +39,10 @@ def test_unaligned_k_linear(mxq, M, K):
     check_gemm(out, y_ref, S, f"linear M={M} K={K}")
 
 
-@pytest.mark.parametrize("M", [130, 1000])
+@pytest.mark.parametrize("M", [100, 130, 1000])
 def test_linear_many_rows(mxq, M):
+    """Quantiser + GEMM (M = 100) and one launch of the quantising CTA-pair
+    GEMM (M > 128), K = 576 with its 64-wide last group."""
     K = 576
     x = W.bf16_normal((M, K), seed=3200 + M)
     w, sw = oracle_weights(1, 512, K, seed=3300)
