@@ -182,7 +182,8 @@ def mxq_linear_workspace_bytes(M, N, K):
 
 
 def mxq_linear(x, w, w_sf, out=None, ws=None, stream=None):
-    """x bf16 [M, K], w uint8 [N, K], w_sf prepared (B=1) -> out bf16 [M, N]."""
+    """x bf16 [M, K], w uint8 [N, K], w_sf prepared (B=1) -> out bf16 [M, N]
+    (one launch for M <= 32 and for M > 128; quantiser + GEMM in between)."""
     M, K = x.shape
     N = w.shape[-2]
     if out is None:
@@ -244,7 +245,9 @@ def mxq_wo_a_workspace_bytes(T, G, D, N):
 
 def mxq_wo_a(x, pos, cos, sin, w, w_sf, R=64, out=None, ws=None, err_flag=None, stream=None):
     """The wo_a projection in one library call: x bf16 [T, G, D] -> out bf16 [T, G, N]
-    (one fused launch for T <= 32; quantiser + GEMM through `ws` otherwise)."""
+    (one launch for T <= 32 and for T > 128, where the GEMM quantises x itself;
+    quantiser + GEMM in between).  `ws` (mxq_wo_a_workspace_bytes) is allocated
+    when not given; concurrent calls need distinct workspaces."""
     T, G, D = x.shape
     N = w.shape[1]
     if out is None:
