@@ -168,6 +168,10 @@ def test_gemm_exact_rational_brute_force():
                 ex = O.dot_exact(a[t, g], sa[t, g], w[g, n], sw[g, n])
                 # fp64 accumulation of exact products: error <= K * 2^-53 * S
                 assert abs(Fraction(y[t, g, n]) - ex) <= Fraction(K) * Fraction(2) ** -53 * Fraction(S[t, g, n])
+                # S is the sum of the magnitudes of the same exact products
+                ex_abs = sum(abs(O.dot_exact(a[t, g, k:k + 1], sa[t, g, k // 128:], w[g, n, k:k + 1],
+                                             sw[g, n, k // 128:])) for k in range(K))
+                assert abs(Fraction(S[t, g, n]) - ex_abs) <= Fraction(K) * Fraction(2) ** -53 * ex_abs
 
 
 def test_gemm_special_cases():

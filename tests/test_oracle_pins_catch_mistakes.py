@@ -1,0 +1,159 @@
+"""The oracle's pins are strong enough to catch plausible mistakes.
+
+Each case below plants one mistake in a private copy of the oracle's source
+(a dropped term, a flipped sign, an off-by-one exponent or bias, a wrong
+index or operand, a wrong rounding rule) and runs the pins of
+test_oracle_encodings.py and test_oracle_path.py against that copy: at least
+one pin has to fail.  The unmodified copy has to pass all of them, which
+checks the harness itself.  Nothing here touches the oracle that the other
+tests import.
+"""
+
+import importlib.util
+import os
+import types
+
+import numpy as np
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ORACLE_PATH = os.path.join(os.path.dirname(HERE), "oracle", "mx_oracle.py")
+PIN_FILES = ("test_oracle_encodings.py", "test_oracle_path.py")
+
+ROPE_X0 = "x0 = x_f32[t, :, D - R:D - half].astype(np.float32)"
+ROPE_X1 = "x1 = x_f32[t, :, D - half:D].astype(np.float32)"
+ROPE_Y0 = "y[t, :, D - R:D - half] = (x0 * c) + (x1 * s)"
+ROPE_Y1 = "y[t, :, D - half:D] = (x1 * c) - (x0 * s)"
+
+# (name, [(text in the oracle, replacement), ...]); every text occurs once.
+MISTAKES = [
+    # E4M3 decode
+    ("e4m3_subnormal_quantum_2^-10", [("mag = M * 2.0 ** -9", "mag = M * 2.0 ** -10")]),
+    ("e4m3_exponent_bias_8", [("2.0 ** (E - 7)\n    return -mag", "2.0 ** (E - 8)\n    return -mag")]),
+    ("e4m3_mantissa_over_16", [("(1.0 + M / 8.0)", "(1.0 + M / 16.0)")]),
+    ("e4m3_no_nan_code", [("if E == 0xF and M == 0x7:", "if False:")]),
+    # E4M3 encode
+    ("encode_ties_away_from_zero", [("& (_POS_CODES[lo] % 2 == 0))", "& False)")]),
+    ("encode_ties_to_odd", [("_POS_CODES[lo] % 2 == 0", "_POS_CODES[lo] % 2 == 1")]),
+    ("encode_truncates", [("pick_lo = (d_lo < d_hi) | ((d_lo == d_hi) & (_POS_CODES[lo] % 2 == 0))",
+                           "pick_lo = d_hi > 0")]),
+    ("encode_overflow_to_nan", [("np.where(a >= E4M3_MAX, 0x7E, code)", "np.where(a > E4M3_MAX, 0x7F, code)")]),
+    ("encode_drops_sign_of_zero", [("code | np.where(neg, 0x80, 0)", "code | np.where(neg & (code != 0), 0x80, 0)")]),
+    # E8M0 scale rule
+    ("scale_threshold_inclusive", [("(m > 0.875)", "(m >= 0.875)")]),
+    ("scale_exponent_off_by_one", [("- 9 + (m > 0.875)", "- 8 + (m > 0.875)")]),
+    ("scale_max_256_not_448", [("(m > 0.875)", "(m > 0.5)")]),
+    ("scale_zero_group_not_min", [("e = np.where(amax == 0.0, -127, e)", "pass")]),
+    ("scale_not_clamped", [("return np.clip(e, -127, 127)", "return e")]),
+    # inverse RoPE
+    ("rope_forward_not_inverse", [(ROPE_Y0, ROPE_Y0.replace("+ (x1", "- (x1")),
+                                  (ROPE_Y1, ROPE_Y1.replace("- (x0", "+ (x0"))]),
+    ("rope_on_first_R_elements", [(ROPE_X0, "x0 = x_f32[t, :, 0:half].astype(np.float32)"),
+                                  (ROPE_X1, "x1 = x_f32[t, :, half:R].astype(np.float32)"),
+                                  (ROPE_Y0, ROPE_Y0.replace("D - R:D - half", "0:half")),
+                                  (ROPE_Y1, ROPE_Y1.replace("D - half:D", "half:R"))]),
+    ("rope_interleaved_pairs", [(ROPE_X0, "x0 = x_f32[t, :, D - R:D:2].astype(np.float32)"),
+                                (ROPE_X1, "x1 = x_f32[t, :, D - R + 1:D:2].astype(np.float32)"),
+                                (ROPE_Y0, ROPE_Y0.replace("D - R:D - half", "D - R:D:2")),
+                                (ROPE_Y1, ROPE_Y1.replace("D - half:D", "D - R + 1:D:2"))]),
+    ("rope_cos_sin_swapped", [(ROPE_Y0, "y[t, :, D - R:D - half] = (x0 * s) + (x1 * c)"),
+                              (ROPE_Y1, "y[t, :, D - half:D] = (x1 * s) - (x0 * c)")]),
+    ("rope_table_row_by_token", [("p = int(pos[t])", "p = t")]),
+    ("rope_output_rounded_to_bf16", [("        y[t, :, D - half:D] = (x1 * c) - (x0 * s)\n    return y",
+                                      "        y[t, :, D - half:D] = (x1 * c) - (x0 * s)\n"
+                                      "    return bf16_bits_to_f32(bf16_rne_bits(y.astype(np.float64)))")]),
+    ("rope_skipped", [("y = inverse_rope_rows(x, pos, cos_bits, sin_bits, R)", "y = x")]),
+    # group quantisation
+    ("quant_scale_bias_128", [("scales[..., kg] = (e + 127)", "scales[..., kg] = (e + 128)")]),
+    ("quant_multiplies_by_scale", [("np.ldexp(blk, -e[..., None])", "np.ldexp(blk, e[..., None])")]),
+    ("quant_signed_amax", [("np.max(np.abs(blk), axis=-1)", "np.max(blk, axis=-1)")]),
+    ("quant_group_64", [("GROUP = 128", "GROUP = 64")]),
+    # MX values, dequantisation
+    ("scale_index_k_mod_groups", [("np.repeat(np.asarray(scales), GROUP, axis=-1)",
+                                   "np.tile(np.asarray(scales), GROUP)")]),
+    ("e8m0_bias_128", [("sc - 127)", "sc - 128)")]),
+    ("e8m0_ff_not_nan", [("return np.where(sc == 255, np.nan, val)", "return val")]),
+    ("bf16_truncates", [("n = np.rint(np.ldexp(a, -q))", "n = np.floor(np.ldexp(a, -q))")]),
+    ("bf16_no_subnormal_quantum", [("q = np.maximum(E.astype(np.int64) - 8, -133)", "q = E.astype(np.int64) - 8")]),
+    ("bf16_nine_bits", [("q = np.maximum(E.astype(np.int64) - 8, -133)", "q = np.maximum(E.astype(np.int64) - 9, -133)")]),
+    # GEMM
+    ("gemm_first_group_weight_for_all", [("A[:, g, :] @ W[g].T", "A[:, g, :] @ W[0].T")]),
+    ("gemm_weight_read_as_k_by_n", [("A[:, g, :] @ W[g].T", "A[:, g, :] @ W[g].reshape(K, N)")]),
+    ("gemm_abs_sum_of_result", [("np.abs(A[:, g, :]) @ np.abs(W[g]).T", "np.abs(A[:, g, :] @ W[g].T)")]),
+    ("gemm_abs_sum_drops_weight_abs", [("np.abs(A[:, g, :]) @ np.abs(W[g]).T", "np.abs(A[:, g, :]) @ W[g].T")]),
+    ("linear_skips_activation_quant", [("    y, S = bmm_a8w8_ref(a_codes[:, None, :]",
+                                        "    a_codes, a_scales = group_quant_rows(x.astype(np.float32) * 1.0)\n"
+                                        "    a_scales = a_scales + 1\n"
+                                        "    y, S = bmm_a8w8_ref(a_codes[:, None, :]")]),
+    # tolerance, scale conversion
+    ("ulp_off_by_one", [("ex = np.maximum(E.astype(np.int64) - 1, -126) - 7",
+                         "ex = np.maximum(E.astype(np.int64) - 1, -126) - 8")]),
+    ("tolerance_relative_1e-4", [("1e-5 * np.asarray(S", "1e-4 * np.asarray(S")]),
+    ("f32_scale_accepts_non_powers", [("& (m == 0.5) ", "")]),
+    ("f32_scale_bias_128", [("np.where(ok, k + 127, 255)", "np.where(ok, k + 128, 255)")]),
+    ("f32_scale_range_128", [("(k >= -127) & (k <= 127)", "(k >= -128) & (k <= 127)")]),
+]
+
+
+def _oracle_copy(edits):
+    with open(ORACLE_PATH) as f:
+        src = f.read()
+    for old, new in edits:
+        assert src.count(old) == 1, f"planted text not found exactly once: {old!r}"
+        src = src.replace(old, new)
+    mod = types.ModuleType("mx_oracle_planted")
+    mod.__file__ = ORACLE_PATH
+    exec(compile(src, ORACLE_PATH, "exec"), mod.__dict__)
+    return mod
+
+
+def _load_pins():
+    mods = []
+    for name in PIN_FILES:
+        spec = importlib.util.spec_from_file_location("pins_" + name[:-3], os.path.join(HERE, name))
+        mod = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(mod)
+        mods.append(mod)
+    return mods
+
+
+PINS = _load_pins()
+
+
+def _cases(mod):
+    for name in sorted(n for n in dir(mod) if n.startswith("test_")):
+        fn = getattr(mod, name)
+        params = [m for m in getattr(fn, "pytestmark", []) if m.name == "parametrize"]
+        if params:
+            for v in params[0].args[1]:
+                yield name, (lambda fn=fn, v=v: fn(v))
+        else:
+            yield name, fn
+
+
+def _failing_pins(oracle, stop_at_first):
+    failed = []
+    for mod in PINS:
+        saved = mod.O
+        mod.O = oracle
+        try:
+            for name, call in _cases(mod):
+                try:
+                    with np.errstate(all="ignore"):
+                        call()
+                except Exception:
+                    failed.append(name)
+                    if stop_at_first:
+                        return failed
+        finally:
+            mod.O = saved
+    return failed
+
+
+def test_unmodified_copy_passes_every_pin():
+    assert _failing_pins(_oracle_copy([]), stop_at_first=False) == []
+
+
+@pytest.mark.parametrize("edits", [m[1] for m in MISTAKES], ids=[m[0] for m in MISTAKES])
+def test_planted_mistake_fails_a_pin(edits):
+    assert _failing_pins(_oracle_copy(edits), stop_at_first=True), "no pin caught this mistake"
