@@ -106,7 +106,8 @@ int mxq_arch_supported(int major, int minor);
  *   e = smallest integer with amax <= 448 * 2^e, clamped to [-127, 127]
  *       (amax == 0 gives -127); scale byte = e + 127;
  *   code = E4M3 round-to-nearest-even, saturating, of y * 2^-e.
- * D % 16 == 0, D >= 16.  T == 0 is a no-op.
+ * D % 16 == 0, D >= 16.  T == 0 is a no-op.  T*G*ceil(D/128) >= 2^31 returns
+ * MXQ_ERR_UNSUPPORTED.
  */
 int mxq_inv_rope_group_quant(const void* x_bf16, int64_t T, int32_t G, int32_t D, int32_t R,
                              const int64_t* pos, const void* cos_bf16, const void* sin_bf16,
@@ -150,7 +151,7 @@ size_t mxq_bmm_workspace_bytes(int64_t T, int32_t G, int32_t N, int32_t K);
  *            is accumulated in fp32 on the tensor cores.
  *  ws        workspace of mxq_bmm_workspace_bytes() bytes (may be NULL if 0).
  * Requirements: K % 16 == 0, N % 16 == 0, K <= 65536, G >= 1.  T == 0 is a
- * no-op.
+ * no-op.  T >= 2^31, G > 65535 or N*K >= 2^40 returns MXQ_ERR_UNSUPPORTED.
  */
 int mxq_bmm_a8w8(const uint8_t* a_e4m3, const uint8_t* a_e8m0, const uint8_t* w_e4m3,
                  const uint8_t* w_sf_prepared, void* out_bf16, int64_t T, int32_t G, int32_t N,
@@ -170,7 +171,8 @@ size_t mxq_linear_workspace_bytes(int64_t M, int32_t N, int32_t K);
  * mxq_inv_rope_group_quant with R = 0 and multiplied as mxq_bmm_a8w8 with
  * G = 1: for M <= 32 and for M > 128 in one launch that quantises inside
  * the GEMM, in between through the workspace.  w_sf_prepared from
- * mxq_prepare_weight_scales(.., B=1, N, K).  M == 0 is a no-op.
+ * mxq_prepare_weight_scales(.., B=1, N, K).  M == 0 is a no-op.  K > 65536,
+ * M >= 2^31 or N*K >= 2^40 returns MXQ_ERR_UNSUPPORTED.
  */
 int mxq_linear(const void* x_bf16, const uint8_t* w_e4m3, const uint8_t* w_sf_prepared,
                void* out_bf16, int64_t M, int32_t N, int32_t K, void* ws, size_t ws_bytes,
@@ -197,7 +199,9 @@ size_t mxq_wo_a_workspace_bytes(int64_t T, int32_t G, int32_t D, int32_t N);
  * first) while the MMA pipeline consumes what is ready.  `ws` holds
  * mxq_wo_a_workspace_bytes(T, G, D, N) bytes, 16-byte aligned; calls that
  * may run at the same time need distinct workspaces.  err_flag as in
- * mxq_inv_rope_group_quant.  T == 0 is a no-op.
+ * mxq_inv_rope_group_quant.  T == 0 is a no-op.  D > 65536, G > 65535,
+ * T >= 2^31, N*D >= 2^40 or T*G*ceil(D/128) >= 2^31 returns
+ * MXQ_ERR_UNSUPPORTED.
  */
 int mxq_wo_a(const void* x_bf16, const int64_t* pos, const void* cos_bf16, const void* sin_bf16,
              int64_t cs_ld, int64_t max_pos, const uint8_t* w_e4m3, const uint8_t* w_sf_prepared,

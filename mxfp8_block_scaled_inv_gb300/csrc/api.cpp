@@ -103,6 +103,9 @@ int mxq_inv_rope_group_quant(const void* x_bf16, int64_t T, int32_t G, int32_t D
     return fail(MXQ_ERR_SHAPE, "need T >= 0, G >= 1, D >= 16, R >= 0 (T=%lld G=%d D=%d R=%d)",
                 (long long)T, G, D, R);
   if (D % 16 != 0) return fail(MXQ_ERR_SHAPE, "D %% 16 != 0 (D=%d)", D);
+  // T and T*G first: each factor below 2^31 keeps every product in int64.
+  if (T >= (int64_t)1 << 31 || T * G >= (int64_t)1 << 31 || T * G * kgroups(D) >= (int64_t)1 << 31)
+    return fail(MXQ_ERR_UNSUPPORTED, "T*G*ceil(D/128) must be < 2^31");
   if (T == 0) return ok();
   if (R > 0) {
     if (R % 16 != 0 || R > 128 || R > D)
@@ -122,8 +125,6 @@ int mxq_inv_rope_group_quant(const void* x_bf16, int64_t T, int32_t G, int32_t D
     return fail(MXQ_ERR_ALIGN, "x, q_e4m3 and q_e8m0 must be 16-byte aligned");
   if (err_flag && (reinterpret_cast<uintptr_t>(err_flag) & 3u))
     return fail(MXQ_ERR_ALIGN, "err_flag must be 4-byte aligned");
-  if (T * G * kgroups(D) >= (int64_t)1 << 31)
-    return fail(MXQ_ERR_UNSUPPORTED, "T*G*ceil(D/128) must be < 2^31");
   int sms = 0;
   if (int st = device_check(&sms)) return st;
   return cuda_status(mxq::launch_inv_rope_group_quant(x_bf16, T, G, D, R, pos, cos_bf16, sin_bf16,
@@ -212,12 +213,14 @@ int mxq_linear(const void* x_bf16, const uint8_t* w_e4m3, const uint8_t* w_sf_pr
   if (M < 0 || N < 16 || K < 16 || K % 16 != 0 || N % 16 != 0)
     return fail(MXQ_ERR_SHAPE, "need M >= 0, N >= 16, K >= 16, N %% 16 == 0, K %% 16 == 0 "
                                "(M=%lld N=%d K=%d)", (long long)M, N, K);
+  if (K > 65536) return fail(MXQ_ERR_UNSUPPORTED, "K > 65536");
+  if (M >= ((int64_t)1 << 31) || (int64_t)N * K >= ((int64_t)1 << 40))
+    return fail(MXQ_ERR_UNSUPPORTED, "M or N*K too large");
   if (M == 0) return ok();
   if (!x_bf16 || !w_e4m3 || !w_sf_prepared || !out_bf16)
     return fail(MXQ_ERR_NULL, "a NULL operand pointer");
   if (!aligned16(x_bf16) || !aligned16(w_e4m3) || !aligned16(w_sf_prepared) || !aligned16(out_bf16))
     return fail(MXQ_ERR_ALIGN, "operands must be 16-byte aligned");
-  if (K > 65536) return fail(MXQ_ERR_UNSUPPORTED, "K > 65536");
   if (M <= mxq::kFusedMaxTokens) {
     // Few rows: one launch that quantises x inside the GEMM.
     int sms = 0;
@@ -273,6 +276,8 @@ int mxq_wo_a(const void* x_bf16, const int64_t* pos, const void* cos_bf16, const
     return fail(MXQ_ERR_SHAPE, "need T >= 0, G >= 1, D >= 16, R >= 0, N >= 16");
   if (D % 16 != 0 || N % 16 != 0) return fail(MXQ_ERR_SHAPE, "need D %% 16 == 0 and N %% 16 == 0");
   if (D > 65536 || G > 65535) return fail(MXQ_ERR_UNSUPPORTED, "D > 65536 or G > 65535");
+  if (T >= ((int64_t)1 << 31) || (int64_t)N * D >= ((int64_t)1 << 40))
+    return fail(MXQ_ERR_UNSUPPORTED, "T or N*D too large");
   if (T == 0) return ok();
   if (R > 0) {
     if (R % 16 != 0 || R > 128 || R > D)

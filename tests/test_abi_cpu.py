@@ -82,6 +82,12 @@ def test_quant_argument_errors(L):
     assert quant(L, R=64, cos=U) == 3
     assert quant(L, err=ctypes.c_void_p((1 << 20) + 2)) == 3
     assert quant(L, T=0, x=None, q=None, sc=None) == 0  # empty input is a no-op
+    # sizes past the 32-bit index range: rejected before any product can overflow
+    assert quant(L, T=1 << 31) == 4
+    assert quant(L, T=1 << 40, G=1 << 30) == 4
+    assert quant(L, T=1 << 20, G=1 << 9, D=512) == 4      # T*G*KG = 2^31
+    assert quant(L, T=1 << 20, G=1 << 11, D=256) == 4     # T*G = 2^31
+    assert quant(L, T=(1 << 62), G=(1 << 31) - 1) == 4
 
 
 def bmm(L, a=P, asf=P, w=P, wsf=P, out=P, T=4, G=1, N=128, K=256, ws=None, ws_bytes=0):
@@ -99,6 +105,9 @@ def test_bmm_argument_errors(L):
     assert bmm(L, K=65536 + 16) == 4
     assert bmm(L, out=U) == 3
     assert bmm(L, T=0, a=None, out=None) == 0
+    assert bmm(L, T=1 << 31) == 4
+    assert bmm(L, G=65536) == 4
+    assert bmm(L, N=1 << 25, K=1 << 16) == 4                # N*K = 2^41
     assert L.mxq_bmm_workspace_bytes(8192, 8, 1024, 4096) == 0
 
 
@@ -113,6 +122,10 @@ def test_linear_argument_errors(L):
     assert L.mxq_linear(None, P, P, P, 8, 5120, 576, P, need, None) == 1
     assert L.mxq_linear(P, P, P, P, 8, 5120, 570, P, need, None) == 2
     assert L.mxq_linear(P, P, P, P, 0, 5120, 576, None, 0, None) == 0
+    assert L.mxq_linear(P, P, P, P, 1 << 31, 5120, 576, P, 1 << 62, None) == 4
+    assert L.mxq_linear(P, P, P, P, 1 << 62, 5120, 576, P, 1 << 62, None) == 4
+    assert L.mxq_linear(P, P, P, P, 8, 1 << 25, 65536, P, 0, None) == 4   # N*K = 2^41
+    assert L.mxq_linear(P, P, P, P, 8, 5120, 65536 + 16, P, 0, None) == 4
 
 
 def wo_a(L, x=P, pos=P, cos=P, sin=P, cs_ld=32, max_pos=16, w=P, wsf=P, out=P, T=4, G=8, D=4096,
@@ -143,6 +156,11 @@ def test_wo_a_argument_errors(L):
     assert L.mxq_wo_a_workspace_bytes(700, 3, 576, 1024) == (
         (700 * 3 * 576 + 255) // 256 * 256 + jobs * 512 + (jobs * 4 + 255) // 256 * 256)
     assert wo_a(L, T=8192) == 6  # prefill sizes go through the workspace
+    assert wo_a(L, T=1 << 31) == 4
+    assert wo_a(L, T=1 << 62) == 4
+    assert wo_a(L, G=65536) == 4
+    assert wo_a(L, N=1 << 25, D=65536) == 4                 # N*D = 2^41
+    assert wo_a(L, T=1 << 24, G=8, D=4096, ws=P, ws_bytes=1 << 62) == 4  # T*G*KG = 2^32
 
 
 def test_dequant_and_scale_argument_errors(L):
