@@ -172,3 +172,34 @@ def test_pair_form_leaves_padding_untouched(mxq):
     torch.cuda.synchronize()
     assert bool((big[T:] == -7.0).all())
     check_gemm(out, *O.bmm_a8w8_ref(a, sa, w, sw), "pair padding")
+
+
+@pytest.mark.parametrize("T", [5, 257])
+def test_maximum_k(mxq, T):
+    """K = 65536, the largest K the ABI accepts (512 scale groups): the
+    few-token form splits it over a cluster of 8 CTAs, the pair form runs all
+    512 groups through one accumulator."""
+    a, sa, w, sw = random_operands(T, 1, 16, 65536, seed=1500 + T)
+    check_gemm(run_bmm(mxq, a, sa, w, sw), *O.bmm_a8w8_ref(a, sa, w, sw), f"K=65536 T={T}")
+
+
+def _random_codes(rng, shape):
+    c = rng.integers(0, 256, size=shape, dtype=np.uint8)
+    c[(c & 0x7F) == 0x7F] = 0x38  # no NaN codes
+    return c
+
+
+@pytest.mark.parametrize("T", [2, 129])
+def test_maximum_groups(mxq, T):
+    """G = 65535, the largest batch the ABI accepts, in the few-token and the
+    pair form (random codes and scale bytes; sampled tokens for the pair form)."""
+    G, N, K = 65535, 16, 128
+    rng = np.random.Generator(np.random.PCG64(1600 + T))
+    a = _random_codes(rng, (T, G, K))
+    sa = rng.integers(118, 136, size=(T, G, 1), dtype=np.uint8)
+    w = _random_codes(rng, (G, N, K))
+    sw = rng.integers(118, 136, size=(G, N, 1), dtype=np.uint8)
+    out = run_bmm(mxq, a, sa, w, sw)
+    idx = np.arange(T) if T <= 4 else np.array([0, 127, 128, T - 1])
+    check_gemm(out[torch.from_numpy(idx).to(out.device)], *O.bmm_a8w8_ref(a[idx], sa[idx], w, sw),
+               f"G=65535 T={T}")
