@@ -65,3 +65,17 @@ def test_linear_close_to_bf16_dequant_path(mxq):
     ref = (xd.double() @ w_bf16.double().T)
     bound = (xd.double().abs() * 2.0 ** -4) @ w_bf16.double().abs().T + 1e-3
     assert bool(((out.double() - ref).abs() <= bound).all())
+
+
+@pytest.mark.parametrize("M", [1, 100, 200])
+def test_maximum_k_linear(mxq, M):
+    """K = 65536, the largest K the ABI accepts, in each of the three launch
+    forms (fused, quantiser + GEMM, quantising CTA pair)."""
+    K = 65536
+    x = W.bf16_normal((M, K), seed=3500 + M)
+    w, sw = oracle_weights(1, 32, K, seed=3501)
+    xd, wd, swd = to_dev(x, w[0], sw)
+    out = mxq.mxq_linear(xd, wd, mxq.mxq_prepare_weight_scales(swd, K))
+    torch.cuda.synchronize()
+    y_ref, S, _, _ = O.linear_ref(W.bf16_bits(x), w[0], sw[0])
+    check_gemm(out, y_ref, S, f"linear M={M} K=65536")

@@ -162,3 +162,11 @@ def test_empty_input_is_noop(mxq):
     cos, sin = to_dev(*W.rope_cache(4, 64))
     q, sc = mxq.mxq_inv_rope_group_quant(x, pos, cos, sin, 64)
     assert q.shape == (0, 8, 4096) and sc.shape == (0, 8, 32)
+
+
+def test_maximum_row_length(mxq):
+    """D = 65536 (512 scale groups per row, the largest D the ABI accepts) with
+    the widest rotated slice, R = 128."""
+    x, pos, cos, sin = wo_a_inputs(40, 2, 65536, 16, 128, seed=2200, max_pos=5000)
+    q, sc = run(mxq, x, pos, cos, sin, 128)
+    assert_same(q, sc, *oracle_quant(x, pos, cos, sin, 128))

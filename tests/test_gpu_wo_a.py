@@ -241,11 +241,11 @@ def test_pair_quant_repeated_runs_match_two_kernels(mxq):
             check_gemm(out[idx], *O.bmm_a8w8_ref(a, sa, w, sw), "sampled")
 
 
-@pytest.mark.parametrize("T", [8, 160])
+@pytest.mark.parametrize("T", [8, 64, 160])
 def test_maximum_d(mxq, T):
     """D = K = 65536, the largest row the ABI accepts (512 scale groups, the
-    rotated slice in the last one), through the fused decode launch (T = 8)
-    and the quantising CTA-pair launch (T = 160)."""
+    rotated slice in the last one), through the fused decode launch (T = 8),
+    quantiser + GEMM (T = 64) and the quantising CTA-pair launch (T = 160)."""
     x, pos, cos, sin = wo_a_inputs(T, 1, 65536, 16, 64, seed=2100 + T, max_pos=5000)
     w, sw = oracle_weights(1, 16, 65536, seed=2101)
     out, _ = run(mxq, x, pos, cos, sin, w, sw, 64)
