@@ -116,10 +116,12 @@ def _stream(stream):
 
 
 def mxq_version():
+    """Library ABI version, major*10000 + minor*100 + patch (100 = 0.1.0)."""
     return lib().mxq_version()
 
 
 def mxq_arch_supported(major, minor):
+    """True when the library runs on a device of this compute capability (10.3 only)."""
     return bool(lib().mxq_arch_supported(major, minor))
 
 
@@ -144,6 +146,7 @@ def mxq_inv_rope_group_quant(x, pos=None, cos=None, sin=None, R=0, q=None, sc=No
 
 
 def mxq_weight_scale_bytes(B, N, K):
+    """Bytes of the prepared weight scales of B matrices [N, K] (0 for invalid sizes)."""
     return lib().mxq_weight_scale_bytes(B, N, K)
 
 
@@ -158,6 +161,7 @@ def mxq_prepare_weight_scales(w_e8m0, K, out=None, stream=None):
 
 
 def mxq_bmm_workspace_bytes(T, G, N, K):
+    """Workspace bytes of mxq_bmm_a8w8 (0 for every shape)."""
     return lib().mxq_bmm_workspace_bytes(T, G, N, K)
 
 
@@ -178,6 +182,7 @@ def mxq_bmm_a8w8(a, a_sf, w, w_sf, out=None, ws=None, stream=None):
 
 
 def mxq_linear_workspace_bytes(M, N, K):
+    """Workspace bytes of mxq_linear: 0 for M <= 32, else codes, scales and (M > 128) job counters."""
     return lib().mxq_linear_workspace_bytes(M, N, K)
 
 
@@ -221,6 +226,10 @@ def mxq_dequant_bf16(w, w_e8m0, out=None, stream=None):
 
 
 def mxq_scales_f32_to_e8m0(s, out=None, err_flag=None, stream=None):
+    """FP32 power-of-two scales (any shape) -> E8M0 bytes of the same shape.
+
+    A value that is not a positive power of two in [2^-127, 2^127] gives byte
+    0xFF and sets MXQ_DEVERR_SCALE in the optional int32 `err_flag`."""
     n = s.numel()
     if out is None:
         out = torch.empty(s.shape, dtype=torch.uint8, device=s.device)
@@ -230,16 +239,20 @@ def mxq_scales_f32_to_e8m0(s, out=None, err_flag=None, stream=None):
 
 
 def mxq_watchdog_read(clear=False):
+    """The device watchdog word (0: no bounded wait inside a kernel ever ran out)."""
     v = ctypes.c_uint32(0)
     _check("mxq_watchdog_read", lib().mxq_watchdog_read(ctypes.byref(v), 1 if clear else 0))
     return v.value
 
 
 def mxq_watchdog_selftest(limit_ns=1_000_000, stream=None):
+    """Launch a kernel whose only wait never completes; it gives up after
+    `limit_ns` and sets the watchdog word (no fault, the context stays usable)."""
     _check("mxq_watchdog_selftest", lib().mxq_watchdog_selftest(limit_ns, _stream(stream)))
 
 
 def mxq_wo_a_workspace_bytes(T, G, D, N):
+    """Workspace bytes of mxq_wo_a: 0 for T <= 32, else codes, scales and (T > 128) job counters."""
     return lib().mxq_wo_a_workspace_bytes(T, G, D, N)
 
 
