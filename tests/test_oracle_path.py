@@ -104,6 +104,27 @@ def test_inverse_rope_is_rotation_by_minus_angle():
     assert np.all(np.abs(y[:, 0, 32:] - z.imag) <= bound)
 
 
+@pytest.mark.parametrize("R", [16, 128])
+def test_inverse_rope_other_widths(R):
+    """The narrowest and widest rotated slices: only the last R elements move,
+    as pairs (D-R+i, D-R/2+i) rotated by -pos*theta_i, theta_i = 10000^(-2i/R)."""
+    D, h = 256, R // 2
+    x = W.bf16_normal((16, 2, D), seed=40 + R)
+    pos = W.positions_uniform(16, seed=41 + R, max_pos=4096).numpy()
+    cos, sin = W.rope_cache(4096, R)
+    xf = O.bf16_bits_to_f32(W.bf16_bits(x))
+    y = O.inverse_rope_rows(xf, pos, W.bf16_bits(cos), W.bf16_bits(sin), R).astype(np.float64)
+    theta = 10000.0 ** (-2.0 * np.arange(h) / R)
+    ang = pos[:, None, None].astype(np.float64) * theta
+    x0 = xf[:, :, D - R:D - h].astype(np.float64)
+    x1 = xf[:, :, D - h:].astype(np.float64)
+    z = (x0 + 1j * x1) * np.exp(-1j * ang)
+    bound = 2.0 ** -8 * 2 * (np.abs(x0) + np.abs(x1)) + 1e-6
+    assert np.all(np.abs(y[:, :, D - R:D - h] - z.real) <= bound)
+    assert np.all(np.abs(y[:, :, D - h:] - z.imag) <= bound)
+    assert np.array_equal(y[:, :, :D - R], xf[:, :, :D - R].astype(np.float64))
+
+
 def test_rope_of_inverse_rope_round_trip():
     x = W.bf16_normal((16, 4, 192), seed=6)
     pos = W.positions_uniform(16, seed=7, max_pos=32768).numpy()

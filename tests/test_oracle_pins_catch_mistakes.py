@@ -59,6 +59,7 @@ MISTAKES = [
     ("rope_cos_sin_swapped", [(ROPE_Y0, "y[t, :, D - R:D - half] = (x0 * s) + (x1 * c)"),
                               (ROPE_Y1, "y[t, :, D - half:D] = (x1 * s) - (x0 * c)")]),
     ("rope_table_row_by_token", [("p = int(pos[t])", "p = t")]),
+    ("rope_half_fixed_at_32", [("half = R // 2", "half = 32")]),
     ("rope_output_rounded_to_bf16", [("        y[t, :, D - half:D] = (x1 * c) - (x0 * s)\n    return y",
                                       "        y[t, :, D - half:D] = (x1 * c) - (x0 * s)\n"
                                       "    return bf16_bits_to_f32(bf16_rne_bits(y.astype(np.float64)))")]),
@@ -68,6 +69,8 @@ MISTAKES = [
     ("quant_multiplies_by_scale", [("np.ldexp(blk, -e[..., None])", "np.ldexp(blk, e[..., None])")]),
     ("quant_signed_amax", [("np.max(np.abs(blk), axis=-1)", "np.max(blk, axis=-1)")]),
     ("quant_group_64", [("GROUP = 128", "GROUP = 64")]),
+    ("quant_amax_over_whole_row", [("amax = np.max(np.abs(blk), axis=-1)",
+                                    "amax = np.max(np.abs(y.astype(np.float64)), axis=-1)")]),
     # MX values, dequantisation
     ("scale_index_k_mod_groups", [("np.repeat(np.asarray(scales), GROUP, axis=-1)",
                                    "np.tile(np.asarray(scales), GROUP)")]),
@@ -90,6 +93,8 @@ MISTAKES = [
                          "ex = np.maximum(E.astype(np.int64) - 1, -126) - 8")]),
     ("tolerance_relative_1e-4", [("1e-5 * np.asarray(S", "1e-4 * np.asarray(S")]),
     ("f32_scale_accepts_non_powers", [("& (m == 0.5) ", "")]),
+    ("f32_scale_accepts_negative", [("np.isfinite(s) & (s > 0) &", "np.isfinite(s) & (s != 0) &"),
+                                    ("m, E = np.frexp(s)\n", "m, E = np.frexp(np.abs(s))\n")]),
     ("f32_scale_bias_128", [("np.where(ok, k + 127, 255)", "np.where(ok, k + 128, 255)")]),
     ("f32_scale_range_128", [("(k >= -127) & (k <= 127)", "(k >= -128) & (k <= 127)")]),
 ]
