@@ -72,6 +72,14 @@ def test_e4m3_encode_saturates():
     assert list(O.e4m3_encode(v)) == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE]
 
 
+def test_e4m3_encode_nan_gives_a_nan_code():
+    """NaN has a code of its own in e4m3fn (S.1111.111); encoding keeps it NaN
+    rather than saturating it to +-448."""
+    codes = O.e4m3_encode(np.array([np.nan, -np.nan, np.nan * 0.0]))
+    assert all(int(c) & 0x7F == 0x7F for c in codes)
+    assert np.isnan(O.e4m3_decode(codes)).all()
+
+
 @pytest.mark.parametrize("row", read_table("e8m0_scale_handworked.txt"), ids=lambda r: r[0])
 def test_scale_rule_handworked(row):
     amax, byte = parse_float(row[0]), int(row[1])

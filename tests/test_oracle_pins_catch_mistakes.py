@@ -38,6 +38,7 @@ MISTAKES = [
     ("encode_truncates", [("pick_lo = (d_lo < d_hi) | ((d_lo == d_hi) & (_POS_CODES[lo] % 2 == 0))",
                            "pick_lo = d_hi > 0")]),
     ("encode_overflow_to_nan", [("np.where(a >= E4M3_MAX, 0x7E, code)", "np.where(a > E4M3_MAX, 0x7F, code)")]),
+    ("encode_nan_not_kept", [("    code = np.where(np.isnan(v), 0x7F, code)\n", "")]),
     ("encode_drops_sign_of_zero", [("code | np.where(neg, 0x80, 0)", "code | np.where(neg & (code != 0), 0x80, 0)")]),
     # E8M0 scale rule
     ("scale_threshold_inclusive", [("(m > 0.875)", "(m >= 0.875)")]),
