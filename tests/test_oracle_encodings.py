@@ -99,7 +99,8 @@ def test_scale_rule_brute_force():
     rng = np.random.Generator(np.random.PCG64(11))
     bits = rng.integers(0, 0x7F800000, size=20_000, dtype=np.uint32)  # all finite fp32 >= 0
     amax = bits.view(np.float32).astype(np.float64)
-    amax = np.concatenate([amax, [0.0, 448.0, 448.00003, 1.0, 2.0 ** -149, 3.4e38]])
+    # beyond fp32 too: the clamp at 127 is part of the rule's definition
+    amax = np.concatenate([amax, [0.0, 448.0, 448.00003, 1.0, 2.0 ** -149, 3.4e38, 2.0 ** 200, 1e300]])
     e = O.e8m0_exponent(amax)
     for a, ee in zip(amax, e):
         assert ee == _scale_by_definition(a), a

@@ -9,16 +9,9 @@ checks the harness itself.  Nothing here touches the oracle that the other
 tests import.
 """
 
-import importlib.util
-import os
-import types
-
-import numpy as np
 import pytest
 
-HERE = os.path.dirname(os.path.abspath(__file__))
-ORACLE_PATH = os.path.join(os.path.dirname(HERE), "oracle", "mx_oracle.py")
-PIN_FILES = ("test_oracle_encodings.py", "test_oracle_path.py")
+from pins_harness import failing_pins, oracle_copy
 
 ROPE_X0 = "x0 = x_f32[t, :, D - R:D - half].astype(np.float32)"
 ROPE_X1 = "x1 = x_f32[t, :, D - half:D].astype(np.float32)"
@@ -101,65 +94,10 @@ MISTAKES = [
 ]
 
 
-def _oracle_copy(edits):
-    with open(ORACLE_PATH) as f:
-        src = f.read()
-    for old, new in edits:
-        assert src.count(old) == 1, f"planted text not found exactly once: {old!r}"
-        src = src.replace(old, new)
-    mod = types.ModuleType("mx_oracle_planted")
-    mod.__file__ = ORACLE_PATH
-    exec(compile(src, ORACLE_PATH, "exec"), mod.__dict__)
-    return mod
-
-
-def _load_pins():
-    mods = []
-    for name in PIN_FILES:
-        spec = importlib.util.spec_from_file_location("pins_" + name[:-3], os.path.join(HERE, name))
-        mod = importlib.util.module_from_spec(spec)
-        spec.loader.exec_module(mod)
-        mods.append(mod)
-    return mods
-
-
-PINS = _load_pins()
-
-
-def _cases(mod):
-    for name in sorted(n for n in dir(mod) if n.startswith("test_")):
-        fn = getattr(mod, name)
-        params = [m for m in getattr(fn, "pytestmark", []) if m.name == "parametrize"]
-        if params:
-            for v in params[0].args[1]:
-                yield name, (lambda fn=fn, v=v: fn(v))
-        else:
-            yield name, fn
-
-
-def _failing_pins(oracle, stop_at_first):
-    failed = []
-    for mod in PINS:
-        saved = mod.O
-        mod.O = oracle
-        try:
-            for name, call in _cases(mod):
-                try:
-                    with np.errstate(all="ignore"):
-                        call()
-                except Exception:
-                    failed.append(name)
-                    if stop_at_first:
-                        return failed
-        finally:
-            mod.O = saved
-    return failed
-
-
 def test_unmodified_copy_passes_every_pin():
-    assert _failing_pins(_oracle_copy([]), stop_at_first=False) == []
+    assert failing_pins(oracle_copy([]), stop_at_first=False) == []
 
 
 @pytest.mark.parametrize("edits", [m[1] for m in MISTAKES], ids=[m[0] for m in MISTAKES])
 def test_planted_mistake_fails_a_pin(edits):
-    assert _failing_pins(_oracle_copy(edits), stop_at_first=True), "no pin caught this mistake"
+    assert failing_pins(oracle_copy(edits), stop_at_first=True), "no pin caught this mistake"
