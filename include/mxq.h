@@ -246,11 +246,13 @@ int mxq_scales_f32_to_e8m0(const float* s, int64_t n, uint8_t* out, int32_t* err
  * must never call cudaMalloc/cudaFree (they can synchronise the device) and
  * whose device memory was reserved up front by another component.
  *
- * Same operation, arguments and results as mxq_linear.  Instead of a
- * caller-provided workspace it uses a fixed scratch array that the library
- * keeps in the device memory of every GPU it is loaded on, until the process
- * exits.  The call allocates nothing.
- *  - Limit: the quantised activation must fit the array:
+ * Same operation, arguments, argument rules and results as mxq_linear; every
+ * argument is checked before anything is enqueued.  Up to 32 rows it is
+ * mxq_linear's single launch, which needs no scratch.  Above that, instead of
+ * a caller-provided workspace it uses a fixed scratch array (quantiser, then
+ * GEMM) that the library keeps in the device memory of every GPU it is
+ * loaded on, until the process exits.  The call allocates nothing.
+ *  - Limit (M > 32): the quantised activation must fit the array:
  *    round_up(M*K, 256) + round_up(M*ceil(K/128), 256) <= MXQ_NOALLOC_SCRATCH_BYTES
  *    (for example M <= 7219 rows at K = 576, 1806 at K = 2304); larger sizes return
  *    MXQ_ERR_WORKSPACE and launch nothing.

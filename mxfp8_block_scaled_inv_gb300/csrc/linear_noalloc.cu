@@ -64,9 +64,23 @@ int scratch_on_current_device(uint8_t** out) {
 extern "C" int mxq_linear_noalloc(const void* x_bf16, const uint8_t* w_e4m3,
                                   const uint8_t* w_sf_prepared, void* out_bf16, int64_t M,
                                   int32_t N, int32_t K, mxq_stream_t stream) {
+  // Every argument rule of mxq_linear, checked before anything is enqueued.
   if (M < 0 || N < 16 || K < 16 || K % 16 != 0 || N % 16 != 0)
     return mxq::set_error(MXQ_ERR_SHAPE, "need M >= 0, N >= 16, K >= 16, N % 16 == 0, K % 16 == 0");
+  if (K > 65536) return mxq::set_error(MXQ_ERR_UNSUPPORTED, "K > 65536");
+  if (M >= ((int64_t)1 << 31) || (int64_t)N * K >= ((int64_t)1 << 40))
+    return mxq::set_error(MXQ_ERR_UNSUPPORTED, "M or N*K too large");
   if (M == 0) return mxq::set_error(MXQ_OK, "");
+  if (!x_bf16 || !w_e4m3 || !w_sf_prepared || !out_bf16)
+    return mxq::set_error(MXQ_ERR_NULL, "a NULL operand pointer");
+  if (((reinterpret_cast<uintptr_t>(x_bf16) | reinterpret_cast<uintptr_t>(w_e4m3) |
+        reinterpret_cast<uintptr_t>(w_sf_prepared) | reinterpret_cast<uintptr_t>(out_bf16)) &
+       15u) != 0)
+    return mxq::set_error(MXQ_ERR_ALIGN, "operands must be 16-byte aligned");
+  // Up to 32 rows the linear is one launch that quantises x inside the GEMM
+  // and needs no scratch at all.
+  if (M <= mxq::kFusedMaxTokens)
+    return mxq_linear(x_bf16, w_e4m3, w_sf_prepared, out_bf16, M, N, K, nullptr, 0, stream);
   // Scratch layout: codes [M, K] (256-byte aligned), then scale bytes [M, ceil(K/128)].
   const size_t codes_bytes = round256((size_t)M * (size_t)K);
   const size_t scale_bytes = round256((size_t)M * (size_t)((K + 127) / 128));
@@ -74,14 +88,14 @@ extern "C" int mxq_linear_noalloc(const void* x_bf16, const uint8_t* w_e4m3,
     return mxq::set_error(MXQ_ERR_WORKSPACE,
                           "M*K too large for the fixed scratch of mxq_linear_noalloc "
                           "(MXQ_NOALLOC_SCRATCH_BYTES); use mxq_linear with a workspace");
-  if (!x_bf16 || !w_e4m3 || !w_sf_prepared || !out_bf16)
-    return mxq::set_error(MXQ_ERR_NULL, "a NULL operand pointer");
   uint8_t* scratch = nullptr;
   if (int st = scratch_on_current_device(&scratch)) return st;
   uint8_t* codes = scratch;
   uint8_t* scales = scratch + codes_bytes;
   // Both stages overwrite every scratch byte they later read, so nothing has
-  // to be cleared between calls.
+  // to be cleared between calls.  The arguments of both calls were checked
+  // above, so neither returns an argument error after the first has been
+  // enqueued.
   if (int st = mxq_inv_rope_group_quant(x_bf16, M, 1, K, 0, nullptr, nullptr, nullptr, 0, 0, codes,
                                         scales, nullptr, stream))
     return st;

@@ -245,6 +245,39 @@ def test_linear_against_bf16_dequant_path():
     assert np.all(np.abs(y - y_bf16path) <= bound)
 
 
+def test_linear_handworked():
+    """Hand-worked MXFP8 linear (tests/golden/linear_handworked.txt): the
+    activation is quantised before the product (a tie rounded to the even
+    code, a value rounded up to the next code, a partial 32-wide last group
+    with its own scale), so y differs from the BF16 x times W product."""
+    sec = read_sections("linear_handworked.txt")
+    M, K, N = 2, 160, 3
+    x = torch.zeros((M, K), dtype=torch.float32)
+    for r, k, v in sec["x"]:
+        x[int(r), int(k)] = float(v)
+    x_bits = W.bf16_bits(x.to(torch.bfloat16))
+    w = np.zeros((N, K), dtype=np.uint8)
+    w[0, :] = 0x38
+    w[1, 1] = 0x38
+    w[2, 132] = 0x38
+    sw = np.array([[127, 127], [127, 127], [127, 130]], dtype=np.uint8)
+    y, S, a_codes, a_scales = O.linear_ref(x_bits, w, sw)
+    want_codes = np.zeros((M, K), dtype=np.uint8)
+    for r, k, c in sec["a_codes"]:
+        want_codes[int(r), int(k)] = int(c, 16)
+    want_scales = np.array([[int(b) for b in row[1:]] for row in sec["a_scales"]], dtype=np.uint8)
+    want_y = np.zeros((M, N))
+    want_S = np.zeros((M, N))
+    for r, n, v in sec["y"]:
+        want_y[int(r), int(n)] = float(v)
+    for r, n, v in sec["S"]:
+        want_S[int(r), int(n)] = float(v)
+    assert np.array_equal(a_codes, want_codes)
+    assert np.array_equal(a_scales, want_scales)
+    assert np.array_equal(y, want_y)
+    assert np.array_equal(S, want_S)
+
+
 def test_gemm_tolerance_definition():
     y_ref = np.array([1.0, -3.0, 0.0])
     S = np.array([10.0, 0.0, 1.0])

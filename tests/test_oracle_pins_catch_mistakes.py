@@ -82,6 +82,16 @@ MISTAKES = [
                                         "    a_codes, a_scales = group_quant_rows(x.astype(np.float32) * 1.0)\n"
                                         "    a_scales = a_scales + 1\n"
                                         "    y, S = bmm_a8w8_ref(a_codes[:, None, :]")]),
+    ("linear_uses_unquantised_x", [("    y, S = bmm_a8w8_ref(a_codes[:, None, :], a_scales[:, None, :],\n"
+                                     "                        w_codes[None], w_scales[None])\n"
+                                     "    return y[:, 0, :], S[:, 0, :], a_codes, a_scales",
+                                     "    Wv = mx_values(w_codes, w_scales)\n"
+                                     "    y = x.astype(np.float64) @ Wv.T\n"
+                                     "    S = np.abs(x.astype(np.float64)) @ np.abs(Wv).T\n"
+                                     "    return y, S, a_codes, a_scales")]),
+    ("linear_partial_group_amax_over_128", [("    a_codes, a_scales = group_quant_rows(x)\n",
+                                              "    a_codes, a_scales = group_quant_rows(x)\n"
+                                              "    a_scales[:, -1] = np.maximum(a_scales[:, -1], a_scales[:, 0])\n")]),
     # tolerance, scale conversion
     ("ulp_off_by_one", [("ex = np.maximum(E.astype(np.int64) - 1, -126) - 7",
                          "ex = np.maximum(E.astype(np.int64) - 1, -126) - 8")]),

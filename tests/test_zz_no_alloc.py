@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import workloads as W
-from cases import oracle_weights, to_dev
+from cases import check_gemm, oracle_weights, to_dev
 from oracle import mx_oracle as O
 
 
@@ -42,12 +42,18 @@ def _noalloc(mxq, x, w, wsf):
     return out
 
 
+# (M, K, seed): two calls in a row share the array (larger, then smaller
+# problem, other inputs); M = 8 and 3 take the single fused launch, which
+# needs no scratch; M = 100 and 7219 go through the array, and 7219 rows at
+# K = 576 (4,158,144 code bytes + 36,095 scale bytes, each rounded up to 256)
+# fill it to its last byte.
+CASES = [(8, 2304, 4100), (3, 576, 4200), (100, 2304, 4300), (7219, 576, 4400), (40, 576, 4500)]
+
+
 @pytest.mark.gpu
-def test_noalloc_matches_linear_on_two_calls_in_a_row(mxq):
-    # Two different problems back to back: the second call reuses the array
-    # the first one filled (larger, then smaller), with other inputs.
-    for M, K, seed in [(8, 2304, 4100), (3, 576, 4200)]:
-        N = 5120
+def test_noalloc_matches_oracle_and_linear_on_calls_in_a_row(mxq):
+    N = 5120
+    for M, K, seed in CASES:
         x = W.bf16_normal((M, K), seed=seed)
         w, sw = oracle_weights(1, N, K, seed=seed + 1)
         xd, wd, swd = to_dev(x, w[0], sw)
@@ -55,11 +61,14 @@ def test_noalloc_matches_linear_on_two_calls_in_a_row(mxq):
         got = _noalloc(mxq, xd, wd, wsf)
         ref = mxq.mxq_linear(xd, wd, wsf)
         torch.cuda.synchronize()
-        # Tolerance of the GEMM parity tests, around the existing entry point's output.
-        _, S, _, _ = O.linear_ref(W.bf16_bits(x), w[0], sw[0])
+        # Against the oracle (activation group quantisation, then the fp64
+        # block-scaled GEMM), at the GEMM parity tolerance.
+        y_ref, S, _, _ = O.linear_ref(W.bf16_bits(x), w[0], sw[0])
+        check_gemm(got, y_ref, S, f"noalloc M={M} K={K}")
+        # And against the entry point with a caller workspace, within the same tolerance.
         g = got.float().cpu().numpy().astype(np.float64)
         r = ref.float().cpu().numpy().astype(np.float64)
-        assert np.all(np.abs(g - r) <= O.gemm_tolerance(r, S)), f"M={M} K={K}"
+        assert np.all(np.abs(g - r) <= O.gemm_tolerance(y_ref, S)), f"M={M} K={K}"
 
 
 def test_noalloc_rejects_sizes_beyond_the_scratch():
@@ -74,3 +83,14 @@ def test_noalloc_rejects_sizes_beyond_the_scratch():
     assert b"scratch" in L.mxq_last_error()
     assert L.mxq_linear_noalloc(p, p, p, p, 4, 5120, 570, None) == 2
     assert L.mxq_linear_noalloc(p, p, p, p, 0, 5120, 576, None) == 0
+    # Every rule of mxq_linear is checked before anything is enqueued (without
+    # a GPU, a call that got as far as a launch would report a CUDA or
+    # architecture error instead of these).
+    u = ctypes.c_void_p((1 << 20) + 8)
+    assert L.mxq_linear_noalloc(p, p, p, u, 100, 5120, 576, None) == 3  # misaligned out
+    assert L.mxq_linear_noalloc(p, p, u, p, 1, 5120, 576, None) == 3    # misaligned scales
+    assert L.mxq_linear_noalloc(p, u, p, p, 40, 5120, 576, None) == 3   # misaligned weight
+    assert L.mxq_linear_noalloc(p, p, p, p, 1, 5120, 131072, None) == 4  # K > 65536
+    assert L.mxq_linear_noalloc(p, p, p, p, 0, 5120, 131072, None) == 4  # checked before M == 0
+    assert L.mxq_linear_noalloc(p, p, p, p, 1, 1 << 25, 65536, None) == 4  # N*K >= 2^40
+    assert L.mxq_linear_noalloc(p, p, p, None, 1, 5120, 576, None) == 1
