@@ -309,6 +309,71 @@ def scales_f32_to_e8m0(s: np.ndarray):
 
 
 # --------------------------------------------------------------------------
+# Forward RoPE and insertion of the new KV row into an FP8 or BF16 cache.
+# Functional-fixes page, Purpose: the fused DeepSeek V4 RoPE / KV-insert path
+# must emit the bytes of the platform's FP8 encoding, OCP E4M3 (max 448) on
+# the current architecture; the cache is checked either as BF16 or as FP8
+# with a per-tensor scale ("full-cache per-tensor FP8"), and the RoPE region
+# is where a kernel and a reference can round opposite ways at ties.
+# Readings: the rotation is the forward one of the wo_a cache (+pos*theta_i,
+# rotate-half pairs of the last R elements of a row); the rotated values stay
+# fp32 and are rounded once, to BF16 (query, BF16 cache) or, divided by the
+# per-tensor scale in fp32, to E4M3 (FP8 cache); a negative slot skips the
+# token's cache row.
+# --------------------------------------------------------------------------
+def forward_rope_rows(x_f32: np.ndarray, pos: np.ndarray, cos_bits: np.ndarray,
+                      sin_bits: np.ndarray, R: int) -> np.ndarray:
+    """Rotate the last R elements of each row by +pos*theta_i.
+
+    x_f32: [T, H, D] float32 (widened BF16).  For i < R/2, j0 = D-R+i,
+    j1 = j0+R/2, c = cos[pos][i], s = sin[pos][i]:
+        y[j0] = fl32(fl32(x[j0]*c) - fl32(x[j1]*s))
+        y[j1] = fl32(fl32(x[j1]*c) + fl32(x[j0]*s))
+    (with a = x[j0], b = x[j1], cs = c, sn = s below).
+    Elements before D-R pass through."""
+    y = np.array(x_f32, dtype=np.float32, copy=True)
+    if R == 0:
+        return y
+    T, H, D = y.shape
+    h = R // 2
+    for t in range(T):
+        row = int(pos[t])
+        cs = bf16_bits_to_f32(cos_bits[row, :h])
+        sn = bf16_bits_to_f32(sin_bits[row, :h])
+        a = x_f32[t, :, D - R:D - h].astype(np.float32)
+        b = x_f32[t, :, D - h:D].astype(np.float32)
+        y[t, :, D - R:D - h] = (a * cs) - (b * sn)  # numpy float32: IEEE RN, no FMA
+        y[t, :, D - h:D] = (b * cs) + (a * sn)
+    return y
+
+
+def rope_kv_insert(q_bits, kv_bits, pos, cos_bits, sin_bits, R, slots, cache, scale=None):
+    """Oracle of mxq_rope_kv_insert.
+
+    q_bits [T, H, Dq] and kv_bits [T, Dk]: BF16 bit patterns; pos [T] valid
+    table rows; slots [T] cache rows (negative: no write).  cache: the cache
+    before the call, [num_slots, Dk], uint8 E4M3 codes when `scale` is given,
+    else uint16 BF16 bits.  Returns (q_out bits [T, H, Dq], the cache after the
+    call).  q_out = BF16_RNE(forward RoPE of q); the cache row of token t is
+    E4M3_RNE_satfinite(fl32(rope(kv) / scale)) or BF16_RNE(rope(kv)), written
+    in token order."""
+    q = bf16_bits_to_f32(q_bits)
+    kv = bf16_bits_to_f32(kv_bits)[:, None, :]
+    q_out = bf16_rne_bits(forward_rope_rows(q, pos, cos_bits, sin_bits, R).astype(np.float64))
+    k = forward_rope_rows(kv, pos, cos_bits, sin_bits, R)[:, 0, :]
+    if scale is None:
+        rows = bf16_rne_bits(k.astype(np.float64))
+    else:
+        v = k / np.float32(scale)  # one IEEE fp32 division
+        rows = e4m3_encode(v.astype(np.float64))
+    out = np.array(cache, copy=True)
+    for t in range(len(slots)):
+        if int(slots[t]) >= 0:
+            out[int(slots[t])] = rows[t]
+    return q_out, out
+
+
+# --------------------------------------------------------------------------
 # Exact rational helpers for brute-force pins on tiny shapes.
 # --------------------------------------------------------------------------
 def e4m3_fraction(code: int) -> Fraction:

@@ -15,7 +15,7 @@ import numpy as np
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ORACLE_PATH = os.path.join(os.path.dirname(HERE), "oracle", "mx_oracle.py")
-PIN_FILES = ("test_oracle_encodings.py", "test_oracle_path.py")
+PIN_FILES = ("test_oracle_encodings.py", "test_oracle_path.py", "test_oracle_kv.py")
 
 
 def oracle_source():

@@ -92,6 +92,23 @@ MISTAKES = [
     ("linear_partial_group_amax_over_128", [("    a_codes, a_scales = group_quant_rows(x)\n",
                                               "    a_codes, a_scales = group_quant_rows(x)\n"
                                               "    a_scales[:, -1] = np.maximum(a_scales[:, -1], a_scales[:, 0])\n")]),
+    # forward RoPE and KV-cache insert
+    ("fwd_rope_is_inverse", [("y[t, :, D - R:D - h] = (a * cs) - (b * sn)", "y[t, :, D - R:D - h] = (a * cs) + (b * sn)"),
+                             ("y[t, :, D - h:D] = (b * cs) + (a * sn)", "y[t, :, D - h:D] = (b * cs) - (a * sn)")]),
+    ("fwd_rope_cos_sin_swapped", [("y[t, :, D - R:D - h] = (a * cs) - (b * sn)", "y[t, :, D - R:D - h] = (a * sn) - (b * cs)")]),
+    ("fwd_rope_table_row_by_token", [("row = int(pos[t])", "row = t")]),
+    ("fwd_rope_pairs_adjacent", [("a = x_f32[t, :, D - R:D - h]", "a = x_f32[t, :, D - R:D:2]"),
+                                 ("b = x_f32[t, :, D - h:D]", "b = x_f32[t, :, D - R + 1:D:2]"),
+                                 ("y[t, :, D - R:D - h] = (a * cs) - (b * sn)", "y[t, :, D - R:D:2] = (a * cs) - (b * sn)"),
+                                 ("y[t, :, D - h:D] = (b * cs) + (a * sn)", "y[t, :, D - R + 1:D:2] = (b * cs) + (a * sn)")]),
+    ("kv_scale_multiplied", [("v = k / np.float32(scale)", "v = k * np.float32(scale)")]),
+    ("kv_scale_in_fp64", [("v = k / np.float32(scale)", "v = k.astype(np.float64) / scale")]),
+    ("kv_negative_slot_written", [("if int(slots[t]) >= 0:", "if True:")]),
+    ("kv_not_rotated", [("k = forward_rope_rows(kv, pos, cos_bits, sin_bits, R)[:, 0, :]", "k = kv[:, 0, :]")]),
+    ("q_not_rotated", [("q_out = bf16_rne_bits(forward_rope_rows(q, pos, cos_bits, sin_bits, R).astype(np.float64))",
+                        "q_out = bf16_rne_bits(q.astype(np.float64))")]),
+    ("q_rounded_before_rotation", [("    q = bf16_bits_to_f32(q_bits)\n",
+                                    "    q = bf16_bits_to_f32(q_bits)\n    q = (q * np.float32(1.0000001)).astype(np.float32)\n")]),
     # tolerance, scale conversion
     ("ulp_off_by_one", [("ex = np.maximum(E.astype(np.int64) - 1, -126) - 7",
                          "ex = np.maximum(E.astype(np.int64) - 1, -126) - 8")]),
