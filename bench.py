@@ -303,6 +303,66 @@ def secondary(mxq, device, peaks):
     return out
 
 
+def kv_insert_bench(mxq, device, peaks):
+    """Forward RoPE + KV-cache insert (E4M3 cache, per-tensor scale): a prefill
+    chunk q [8192, 64, 512] / kv [8192, 512] (query out of place and in place),
+    and decode T = 1 / 8 / 64 over 61 layers with distinct caches in one CUDA
+    graph."""
+    import workloads as W
+
+    H, Dh, Rk = 64, 512, 64
+    hbm = peaks["hbm_gbs"]
+    cos, sin = rope_tables(65536, device)
+    scale = torch.tensor([0.0371], dtype=torch.float32, device=device)
+    out = {}
+    T = 8192
+    q = W.bf16_normal_cuda((T, H, Dh), seed=8100, device=device)
+    kv = W.bf16_normal_cuda((T, Dh), seed=8101, std=4.0, device=device)
+    pos = torch.arange(32768, 32768 + T, dtype=torch.int64, device=device)
+    slots = torch.randperm(4 * T, device=device)[:T].to(torch.int64)
+    cache = torch.zeros((4 * T, Dh), dtype=torch.uint8, device=device)
+    q_out = torch.empty_like(q)
+    side = T * (2 * Dh + Dh + 8 + 8 + 2 * Rk)  # kv read, cache row written, pos, slot, cos/sin
+    for name, qo, byt in (("prefill_out_of_place", q_out, 2 * (2 * T * H * Dh) + side),
+                          ("prefill_in_place", q, 2 * (2 * T * H * Rk) + side)):
+        for _ in range(5):
+            mxq.mxq_rope_kv_insert(q, kv, pos, cos, sin, Rk, slots, cache, scale=scale, q_out=qo)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 20
+        a.record()
+        for _ in range(reps):
+            mxq.mxq_rope_kv_insert(q, kv, pos, cos, sin, Rk, slots, cache, scale=scale, q_out=qo)
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / reps
+        out[name] = {"us": round(us, 2), "algorithmic_bytes": byt, "gbs": round(byt / (us * 1e-6) / 1e9, 1),
+                     "hbm_frac": round(byt / (us * 1e-6) / 1e9 / hbm, 3)}
+    del q, kv, q_out, cache
+    torch.cuda.empty_cache()
+    dec = {}
+    layers = 61
+    for T in (1, 8, 64):
+        q = W.bf16_normal_cuda((T, H, Dh), seed=8200 + T, device=device)
+        kv = W.bf16_normal_cuda((T, Dh), seed=8300 + T, std=4.0, device=device)
+        pos = W.positions_uniform_cuda(T, seed=8400 + T, max_pos=65536, device=device)
+        slots = torch.arange(T, dtype=torch.int64, device=device) * 7
+        caches = [torch.zeros((8 * T, Dh), dtype=torch.uint8, device=device) for _ in range(layers)]
+        q_out = torch.empty_like(q)
+
+        def stack():
+            for c in caches:
+                mxq.mxq_rope_kv_insert(q, kv, pos, cos, sin, Rk, slots, c, scale=scale, q_out=q_out)
+
+        us = time_graph(stack, 20) * 1e3 / layers
+        byt = 2 * (2 * T * H * Dh) + T * (2 * Dh + Dh + 8 + 8 + 2 * Rk)
+        dec[str(T)] = {"us_per_layer": round(us, 2), "gbs": round(byt / (us * 1e-6) / 1e9, 1)}
+    out["decode"] = dec
+    out["workload"] = ("q [T,64,512] bf16, kv [T,512] bf16, R=64, E4M3 cache with per-tensor scale; "
+                       "prefill T=8192 at positions 32768.., decode 61 layers in one CUDA graph")
+    return out
+
+
 def stream_100k(mxq, device):
     """100,000-token prefill stream (12 x 8192 + 1696) through 61 wo_a layers."""
     import workloads as W
@@ -764,6 +824,7 @@ def main():
     if not args.no_secondary and rank == 0:
         sec = secondary(mxq, device, peaks)
         sec["stream_100k"] = stream_100k(mxq, device)
+        sec["rope_kv_insert"] = kv_insert_bench(mxq, device, peaks)
     if mxq.mxq_watchdog_read() != 0:
         raise SystemExit("a bounded wait inside a kernel ran out; numbers are not valid")
 

@@ -59,6 +59,11 @@ typedef enum mxq_status {
  * each entry point and the bit is set. */
 #define MXQ_DEVERR_POSITION 0x1  /* a position outside [0, max_pos) */
 #define MXQ_DEVERR_SCALE 0x2     /* an FP32 scale that is not a power of two in range */
+#define MXQ_DEVERR_SLOT 0x4      /* a KV-cache slot at or beyond the number of cache rows */
+
+/* Cache element types of mxq_rope_kv_insert. */
+#define MXQ_CACHE_E4M3 0 /* OCP E4M3 bytes with one per-tensor FP32 scale */
+#define MXQ_CACHE_BF16 1 /* BF16 */
 
 /* Human-readable name of a status code.  Never NULL. */
 const char* mxq_status_string(int status);
@@ -231,6 +236,55 @@ int mxq_dequant_bf16(const uint8_t* w_e4m3, const uint8_t* w_e8m0, void* out_bf1
  */
 int mxq_scales_f32_to_e8m0(const float* s, int64_t n, uint8_t* out, int32_t* err_flag,
                            mxq_stream_t stream);
+
+/*
+ * Forward RoPE of the query and of the new KV row, and insertion of the KV
+ * row into the KV cache, in one kernel.  Functional-fixes page ("[ROCm][DSv4]
+ * Functional fixes for DeepSeek V4 on MI300X/MI325X"), Purpose: the fused
+ * DeepSeek V4 RoPE / KV-insert path must store the bytes of the platform's
+ * FP8 encoding -- OCP E4M3, maximum 448, on the current architecture -- and
+ * the cache is either BF16 or FP8 with one per-tensor scale.  The page's
+ * fused kernel also normalises the query (qnorm); it states neither the norm,
+ * its epsilon nor its weight, so this entry point does not normalise.
+ *
+ *  q_bf16     [T, H, Dq] BF16 query (H may be 0: no query).  q_out_bf16
+ *             [T, H, Dq] BF16 out; it may be q_bf16 itself (in place: then
+ *             only the rotated slice is read and written), but must not
+ *             overlap it otherwise.
+ *  kv_bf16    [T, Dk] BF16, the new KV row of each token.
+ *  pos, cos_bf16, sin_bf16, cs_ld, max_pos, R
+ *             as in mxq_inv_rope_group_quant, but the rotation is the
+ *             forward one: for the rotate-half pairs (D-R+i, D-R/2+i) of the
+ *             last R elements of every query head row and of every KV row,
+ *               y0 = fl32(x0*c - x1*s),  y1 = fl32(x1*c + x0*s)
+ *             (rotation by +p*theta_i; each product is exact in fp32, so
+ *             each value is one rounding).  R is 0 or a multiple of 16 with
+ *             R <= Dk and, when H > 0, R <= Dq.  pos/cos/sin are unused when
+ *             R == 0.
+ *  slot_mapping
+ *             [T] int64: cache row of token t.  A negative slot writes no
+ *             row (padding tokens).  Slots of different tokens must differ.
+ *  kv_cache   [num_slots, Dk]: E4M3 bytes (cache_dtype MXQ_CACHE_E4M3) or
+ *             BF16 (MXQ_CACHE_BF16).  Only the rows named by slot_mapping are
+ *             written.
+ *  kv_scale   device pointer to the per-tensor FP32 scale (E4M3 cache only;
+ *             a positive finite value): the cache byte is the round-to-
+ *             nearest-even, saturating (+-448) E4M3 of fl32(y / *kv_scale).
+ *             The BF16 cache holds bf16_rne(y); the query output is
+ *             bf16_rne(y) (elements outside the slice are copied unchanged).
+ *  err_flag   optional int32 device word: MXQ_DEVERR_POSITION for a token
+ *             whose position is outside [0, max_pos) (its query slices are
+ *             written as zeros and its KV row is not written), and
+ *             MXQ_DEVERR_SLOT for a slot >= num_slots (no row written).
+ * Dq % 16 == 0 (when H > 0), Dk % 16 == 0, Dk >= 16.  T == 0 is a no-op.
+ * T*H*Dq/8 + T*Dk/8 >= 2^31 returns MXQ_ERR_UNSUPPORTED.
+ */
+int mxq_rope_kv_insert(const void* q_bf16, void* q_out_bf16, int64_t T, int32_t H, int32_t Dq,
+                       const void* kv_bf16, int32_t Dk, const int64_t* pos, const void* cos_bf16,
+                       const void* sin_bf16, int64_t cs_ld, int64_t max_pos, int32_t R,
+                       const int64_t* slot_mapping, void* kv_cache, int64_t num_slots,
+                       int32_t cache_dtype, const float* kv_scale, int32_t* err_flag,
+                       mxq_stream_t stream);
 
 /* Size in bytes of the fixed device scratch array behind
  * mxq_linear_noalloc (4 MiB). */

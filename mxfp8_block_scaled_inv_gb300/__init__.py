@@ -22,7 +22,7 @@ __all__ = [
     "mxq_linear_noalloc",
     "mxq_dequant_bf16", "mxq_scales_f32_to_e8m0", "mxq_watchdog_read", "mxq_watchdog_selftest",
     "mxq_arch_supported",
-    "mxq_version", "mxq_wo_a_workspace_bytes", "mxq_wo_a", "wo_a",
+    "mxq_version", "mxq_wo_a_workspace_bytes", "mxq_wo_a", "wo_a", "mxq_rope_kv_insert",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -30,6 +30,9 @@ library_path = os.path.join(HERE, "libmxq.so")
 
 MXQ_DEVERR_POSITION = 0x1
 MXQ_DEVERR_SCALE = 0x2
+MXQ_DEVERR_SLOT = 0x4
+MXQ_CACHE_E4M3 = 0
+MXQ_CACHE_BF16 = 1
 
 
 class MxqLibraryError(RuntimeError):
@@ -67,6 +70,8 @@ _SIGNATURES = {
     "mxq_linear_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp]),
     "mxq_watchdog_selftest": (ctypes.c_int, [ctypes.c_uint64, _vp]),
     "mxq_wo_a_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32]),
+    "mxq_rope_kv_insert": (ctypes.c_int, [_vp, _vp, _i64, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _i64,
+                                          _i64, _i32, _vp, _vp, _i64, _i32, _vp, _vp, _vp]),
     "mxq_wo_a": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _i64, _i32, _i32, _i32,
                                 _i32, _vp, _vp, _sz, _vp]),
 }
@@ -278,3 +283,29 @@ def mxq_wo_a(x, pos, cos, sin, w, w_sf, R=64, out=None, ws=None, err_flag=None, 
 
 
 wo_a = mxq_wo_a
+
+
+def mxq_rope_kv_insert(q, kv, pos, cos, sin, R, slot_mapping, cache, scale=None, q_out=None,
+                       err_flag=None, stream=None):
+    """Forward RoPE of q bf16 [T, H, Dq] (into q_out, default a new tensor;
+    pass q_out=q to rotate in place) and of kv bf16 [T, Dk], whose rows are
+    written to cache[slot_mapping[t]]: uint8 cache [num_slots, Dk] = E4M3 of
+    fl32(y / scale) with `scale` a float32 device tensor of one element, or
+    bf16 cache [num_slots, Dk] = bf16(y).  Returns q_out."""
+    T, H, Dq = q.shape if q is not None else (kv.shape[0], 0, 0)
+    Dk = kv.shape[1]
+    if q is not None and q_out is None:
+        q_out = torch.empty_like(q)
+    if cache.dtype == torch.uint8:
+        dtype = MXQ_CACHE_E4M3
+    elif cache.dtype == torch.bfloat16:
+        dtype = MXQ_CACHE_BF16
+    else:
+        raise MxqError("mxq_rope_kv_insert", 4, "cache must be uint8 (E4M3) or bfloat16")
+    cs_ld = cos.stride(0) if cos is not None else 0
+    max_pos = cos.shape[0] if cos is not None else 0
+    st = lib().mxq_rope_kv_insert(_ptr(q), _ptr(q_out), T, H, Dq, _ptr(kv), Dk, _ptr(pos), _ptr(cos),
+                                  _ptr(sin), cs_ld, max_pos, R, _ptr(slot_mapping), _ptr(cache),
+                                  cache.shape[0], dtype, _ptr(scale), _ptr(err_flag), _stream(stream))
+    _check("mxq_rope_kv_insert", st)
+    return q_out

@@ -22,7 +22,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libmxq.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CU_SOURCES = ["quant.cu", "misc.cu", "bmm.cu", "linear_noalloc.cu"]
+CU_SOURCES = ["quant.cu", "misc.cu", "bmm.cu", "linear_noalloc.cu", "kv_insert.cu"]
 CXX_SOURCES = ["api.cpp"]
 
 

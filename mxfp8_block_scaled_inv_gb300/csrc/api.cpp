@@ -364,6 +364,62 @@ int mxq_scales_f32_to_e8m0(const float* s, int64_t n, uint8_t* out, int32_t* err
                      "scales_f32_to_e8m0 launch");
 }
 
+int mxq_rope_kv_insert(const void* q_bf16, void* q_out_bf16, int64_t T, int32_t H, int32_t Dq,
+                       const void* kv_bf16, int32_t Dk, const int64_t* pos, const void* cos_bf16,
+                       const void* sin_bf16, int64_t cs_ld, int64_t max_pos, int32_t R,
+                       const int64_t* slot_mapping, void* kv_cache, int64_t num_slots,
+                       int32_t cache_dtype, const float* kv_scale, int32_t* err_flag,
+                       mxq_stream_t stream) {
+  if (T < 0 || H < 0 || Dk < 16 || R < 0 || num_slots < 0 || (H > 0 && Dq < 16))
+    return fail(MXQ_ERR_SHAPE, "need T >= 0, H >= 0, Dk >= 16, R >= 0, num_slots >= 0, "
+                               "Dq >= 16 when H > 0 (T=%lld H=%d Dq=%d Dk=%d R=%d)",
+                (long long)T, H, Dq, Dk, R);
+  if (Dk % 16 != 0 || (H > 0 && Dq % 16 != 0))
+    return fail(MXQ_ERR_SHAPE, "need Dk %% 16 == 0 and Dq %% 16 == 0 (Dq=%d Dk=%d)", Dq, Dk);
+  if (cache_dtype != MXQ_CACHE_E4M3 && cache_dtype != MXQ_CACHE_BF16)
+    return fail(MXQ_ERR_UNSUPPORTED, "cache_dtype must be MXQ_CACHE_E4M3 or MXQ_CACHE_BF16");
+  if (R % 16 != 0 || R > Dk || (H > 0 && R > Dq))
+    return fail(MXQ_ERR_UNSUPPORTED, "R must be a multiple of 16, <= Dk and <= Dq (R=%d)", R);
+  // Every factor is below 2^31 here, so the products fit in int64.
+  if (T >= ((int64_t)1 << 31) ||
+      T * ((int64_t)H * (Dq / 8) + Dk / 8) >= ((int64_t)1 << 31))
+    return fail(MXQ_ERR_UNSUPPORTED, "T*H*Dq/8 + T*Dk/8 must be < 2^31");
+  if (T == 0) return ok();
+  if (R > 0) {
+    if (max_pos < 1 || cs_ld < R / 2)
+      return fail(MXQ_ERR_SHAPE, "need max_pos >= 1 and cs_ld >= R/2 (max_pos=%lld cs_ld=%lld)",
+                  (long long)max_pos, (long long)cs_ld);
+    if (cs_ld % 8 != 0) return fail(MXQ_ERR_ALIGN, "cs_ld %% 8 != 0 (cs_ld=%lld)", (long long)cs_ld);
+    if (!pos || !cos_bf16 || !sin_bf16) return fail(MXQ_ERR_NULL, "pos/cos/sin is NULL with R > 0");
+    if (!aligned16(cos_bf16) || !aligned16(sin_bf16) || (reinterpret_cast<uintptr_t>(pos) & 7u))
+      return fail(MXQ_ERR_ALIGN, "cos/sin must be 16-byte aligned and pos 8-byte aligned");
+  }
+  if (!kv_bf16 || !slot_mapping || !kv_cache) return fail(MXQ_ERR_NULL, "kv, slot_mapping or kv_cache is NULL");
+  if (H > 0 && (!q_bf16 || !q_out_bf16)) return fail(MXQ_ERR_NULL, "q or q_out is NULL with H > 0");
+  if (cache_dtype == MXQ_CACHE_E4M3 && !kv_scale) return fail(MXQ_ERR_NULL, "kv_scale is NULL for an E4M3 cache");
+  if (!aligned16(kv_bf16) || !aligned16(kv_cache) || (H > 0 && (!aligned16(q_bf16) || !aligned16(q_out_bf16))))
+    return fail(MXQ_ERR_ALIGN, "q, q_out, kv and kv_cache must be 16-byte aligned");
+  if (H > 0 && q_bf16 != q_out_bf16) {
+    // Distinct query buffers must not overlap (in place is q_out == q exactly).
+    const uintptr_t a = reinterpret_cast<uintptr_t>(q_bf16), b = reinterpret_cast<uintptr_t>(q_out_bf16);
+    const uintptr_t n = (uintptr_t)T * (uintptr_t)H * (uintptr_t)Dq * 2u;
+    if (a < b + n && b < a + n)
+      return fail(MXQ_ERR_SHAPE, "q_out overlaps q without being q itself");
+  }
+  if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) ||
+      (kv_scale && (reinterpret_cast<uintptr_t>(kv_scale) & 3u)) ||
+      (err_flag && (reinterpret_cast<uintptr_t>(err_flag) & 3u)))
+    return fail(MXQ_ERR_ALIGN, "slot_mapping must be 8-byte aligned, kv_scale and err_flag 4-byte aligned");
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  return cuda_status(
+      mxq::launch_rope_kv_insert(q_bf16, q_out_bf16, T, H, Dq, kv_bf16, Dk, pos, cos_bf16, sin_bf16,
+                                 cs_ld, max_pos, R, slot_mapping, kv_cache, num_slots,
+                                 cache_dtype == MXQ_CACHE_E4M3 ? 1 : 0, kv_scale, err_flag, sms,
+                                 static_cast<cudaStream_t>(stream)),
+      "rope_kv_insert launch");
+}
+
 int mxq_watchdog_read(uint32_t* host_value, int clear) {
   if (!host_value) return fail(MXQ_ERR_NULL, "host_value is NULL");
   int sms = 0;

@@ -76,6 +76,16 @@ inline WoaPrefillLayout woa_prefill_layout(int64_t T, int G, int K) {
   return l;
 }
 
+// Forward RoPE of q [T][H][Dq] into q_out (may equal q) and of kv [T][Dk],
+// whose rows go to cache rows slot[t] (E4M3 of fl32(y / *scale) when fp8,
+// else BF16).
+cudaError_t launch_rope_kv_insert(const void* q, void* q_out, int64_t T, int H, int Dq,
+                                  const void* kv, int Dk, const int64_t* pos, const void* cos,
+                                  const void* sin, int64_t cs_ld, int64_t max_pos, int R,
+                                  const int64_t* slot, void* cache, int64_t num_slots, int fp8,
+                                  const float* scale, int32_t* err_flag, int num_sms,
+                                  cudaStream_t s);
+
 cudaError_t watchdog_read(uint32_t* value, bool clear);
 
 // One tiny kernel whose only wait can never be satisfied; it must give up

@@ -69,6 +69,20 @@ int main(void) {
   st = mxq_linear_noalloc(p, p, p, p, 1 << 20, 5120, 576, NULL);
   EXPECT(st == MXQ_ERR_WORKSPACE); /* beyond the fixed scratch */
 
+  st = mxq_linear_noalloc(p, p, p, u, 100, 5120, 576, NULL);
+  EXPECT(st == MXQ_ERR_ALIGN); /* every rule checked before anything is enqueued */
+  st = mxq_linear_noalloc(p, p, p, p, 1, 5120, 131072, NULL);
+  EXPECT(st == MXQ_ERR_UNSUPPORTED);
+
+  /* KV insert: an E4M3 cache needs its per-tensor scale; a BF16 cache does not. */
+  st = mxq_rope_kv_insert(p, p, 4, 2, 512, p, 512, p, p, p, 32, 16, 64, p, p, 8, MXQ_CACHE_E4M3,
+                          NULL, NULL, NULL);
+  EXPECT(st == MXQ_ERR_NULL);
+  st = mxq_rope_kv_insert(p, p, 4, 2, 512, p, 520, p, p, p, 32, 16, 64, p, p, 8, MXQ_CACHE_BF16,
+                          NULL, NULL, NULL);
+  EXPECT(st == MXQ_ERR_SHAPE);
+  EXPECT(MXQ_DEVERR_SLOT == 4);
+
   printf("%d failures\n", failures);
   return failures ? 1 : 0;
 }

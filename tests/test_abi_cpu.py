@@ -187,3 +187,47 @@ def test_weight_scale_bytes(L):
 def test_valid_call_without_device_reports_cuda_error(L):
     assert quant(L) == 7
     assert bmm(L) == 7
+
+
+def kv_insert(L, q=P, q_out=ctypes.c_void_p(1 << 30), T=4, H=2, Dq=512, kv=P, Dk=512, pos=P, cos=P,
+              sin=P, cs_ld=32, max_pos=16, R=64, slot=P, cache=P, num_slots=8, dtype=0, scale=P,
+              err=None):
+    return L.mxq_rope_kv_insert(q, q_out, T, H, Dq, kv, Dk, pos, cos, sin, cs_ld, max_pos, R, slot,
+                                cache, num_slots, dtype, scale, err, None)
+
+
+def test_rope_kv_insert_argument_errors(L):
+    assert kv_insert(L, kv=None) == 1
+    assert kv_insert(L, slot=None) == 1
+    assert kv_insert(L, cache=None) == 1
+    assert kv_insert(L, q=None) == 1
+    assert kv_insert(L, scale=None) == 1                 # E4M3 cache needs its scale
+    assert kv_insert(L, scale=None, dtype=1) != 1        # BF16 cache does not
+    assert kv_insert(L, pos=None) == 1
+    assert kv_insert(L, Dk=8) == 2
+    assert kv_insert(L, Dk=520) == 2
+    assert kv_insert(L, Dq=520) == 2
+    assert kv_insert(L, T=-1) == 2
+    assert kv_insert(L, num_slots=-1) == 2
+    assert kv_insert(L, R=8) == 4
+    assert kv_insert(L, R=528) == 4                      # R > Dk
+    assert kv_insert(L, Dq=256, R=272, Dk=512) == 4      # R > Dq
+    assert kv_insert(L, dtype=2) == 4
+    assert kv_insert(L, cs_ld=36) == 3
+    assert kv_insert(L, cs_ld=16) == 2
+    assert kv_insert(L, kv=U) == 3
+    assert kv_insert(L, q_out=U) == 3
+    assert kv_insert(L, scale=ctypes.c_void_p((1 << 20) + 2)) == 3
+    assert kv_insert(L, slot=ctypes.c_void_p((1 << 20) + 4)) == 3
+    assert kv_insert(L, q_out=ctypes.c_void_p((1 << 20) + 1024)) == 2  # overlaps q, not q itself
+    assert kv_insert(L, T=0, kv=None, cache=None, slot=None) == 0
+    assert kv_insert(L, T=1 << 31) == 4
+    assert kv_insert(L, T=1 << 20, H=64, Dq=512) == 4     # T*H*Dq/8 >= 2^31
+    # H = 0: no query pointers needed
+    assert kv_insert(L, q=None, q_out=None, H=0, Dq=0) != 1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_rope_kv_insert_valid_call_without_device(L):
+    assert kv_insert(L) == 7
+    assert kv_insert(L, q_out=P) == 7  # in place
