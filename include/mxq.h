@@ -323,6 +323,20 @@ int mxq_linear_noalloc(const void* x_bf16, const uint8_t* w_e4m3, const uint8_t*
                        void* out_bf16, int64_t M, int32_t N, int32_t K, mxq_stream_t stream);
 
 /*
+ * Testing aid (the pages have no counterpart): caps the number of CTA pairs
+ * that the many-token GEMM forms launch -- mxq_bmm_a8w8, mxq_wo_a and
+ * mxq_linear above 128 tokens -- for the whole process; 0 (the default)
+ * launches one pair per cluster slot that fits on the device.  Results do
+ * not depend on the cap: every pair walks the work units with a stride of
+ * the pair count, and the one-launch prefill deals its quantisation jobs by
+ * unit, so any grid covers all of them.  That launch is cooperative: all its
+ * pairs are resident together (they wait on each other's job counters), so
+ * a grid that cannot fit is refused rather than left waiting.  Returns the
+ * previous cap; a negative value is taken as 0.
+ */
+int mxq_debug_set_pair_limit(int pairs);
+
+/*
  * Watchdog word of the GEMM kernels on the current device (host call,
  * synchronous).  Every wait inside a kernel is bounded; a wait that runs out
  * sets a bit here and the kernel returns early instead of hanging.  0 means

@@ -23,6 +23,7 @@ __all__ = [
     "mxq_dequant_bf16", "mxq_scales_f32_to_e8m0", "mxq_watchdog_read", "mxq_watchdog_selftest",
     "mxq_arch_supported",
     "mxq_version", "mxq_wo_a_workspace_bytes", "mxq_wo_a", "wo_a", "mxq_rope_kv_insert",
+    "mxq_debug_set_pair_limit",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -69,6 +70,7 @@ _SIGNATURES = {
     "mxq_watchdog_read": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "mxq_linear_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp]),
     "mxq_watchdog_selftest": (ctypes.c_int, [ctypes.c_uint64, _vp]),
+    "mxq_debug_set_pair_limit": (ctypes.c_int, [ctypes.c_int]),
     "mxq_wo_a_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32]),
     "mxq_rope_kv_insert": (ctypes.c_int, [_vp, _vp, _i64, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _i64,
                                           _i64, _i32, _vp, _vp, _i64, _i32, _vp, _vp, _vp]),
@@ -248,6 +250,12 @@ def mxq_watchdog_read(clear=False):
     v = ctypes.c_uint32(0)
     _check("mxq_watchdog_read", lib().mxq_watchdog_read(ctypes.byref(v), 1 if clear else 0))
     return v.value
+
+
+def mxq_debug_set_pair_limit(pairs):
+    """Testing aid: cap the CTA pairs of the many-token GEMM launches (0 = no
+    cap); returns the previous cap."""
+    return lib().mxq_debug_set_pair_limit(int(pairs))
 
 
 def mxq_watchdog_selftest(limit_ns=1_000_000, stream=None):

@@ -420,6 +420,8 @@ int mxq_rope_kv_insert(const void* q_bf16, void* q_out_bf16, int64_t T, int32_t 
       "rope_kv_insert launch");
 }
 
+int mxq_debug_set_pair_limit(int pairs) { return mxq::set_pair_limit(pairs); }
+
 int mxq_watchdog_read(uint32_t* host_value, int clear) {
   if (!host_value) return fail(MXQ_ERR_NULL, "host_value is NULL");
   int sms = 0;

@@ -89,6 +89,10 @@ namespace mxq {
 
 __device__ uint32_t g_watchdog;
 
+// Cap on the CTA pairs of the pair forms (0: one pair per co-resident
+// cluster slot); a testing aid, see mxq_debug_set_pair_limit.
+std::atomic<int> g_pair_limit{0};
+
 namespace {
 
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
@@ -1619,18 +1623,30 @@ cudaError_t launch_cfg(const void* a, const uint8_t* w, BmmArgs args, int num_sm
   // Programmatic dependent launch: the grid may start while the preceding
   // kernel on the stream finishes; it waits (griddepcontrol.wait) before
   // reading anything that kernel produced.
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const int cluster = PAIR ? 2 : args.splits;
   if (cluster > 1) {
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = (unsigned)cluster;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.numAttrs = 2;
+    attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+    attr[cfg.numAttrs].val.clusterDim.x = (unsigned)cluster;
+    attr[cfg.numAttrs].val.clusterDim.y = 1;
+    attr[cfg.numAttrs].val.clusterDim.z = 1;
+    ++cfg.numAttrs;
+  }
+  if (QUANT) {
+    // The quantising pairs wait on job counters that other pairs raise, so
+    // every pair of the grid must be resident at the same time.  A
+    // cooperative launch guarantees that: the grid starts only once all of
+    // it fits beside whatever else runs on the device (a kernel of another
+    // stream holding SMs delays the start instead of stranding pairs that
+    // wait on pairs that cannot start), and a grid that can never fit is
+    // refused at launch.
+    attr[cfg.numAttrs].id = cudaLaunchAttributeCooperative;
+    attr[cfg.numAttrs].val.cooperative = 1;
+    ++cfg.numAttrs;
   }
   int grid = args.units;
   if (PAIR) {
@@ -1648,6 +1664,8 @@ cudaError_t launch_cfg(const void* a, const uint8_t* w, BmmArgs args, int num_sm
       }
       pair_slots[dev & 63].store(slots, std::memory_order_release);
     }
+    const int cap = g_pair_limit.load(std::memory_order_relaxed);
+    if (cap > 0 && cap < slots) slots = cap;
     grid = 2 * (args.units < slots ? args.units : slots);
   } else if (args.persistent) {
     const int slots = num_sms * C::CTAS_PER_SM;
@@ -1762,6 +1780,8 @@ cudaError_t launch_wo_a_prefill(const void* x, const int64_t* pos, const void* c
   if (e != cudaSuccess) return e;
   return launch_cfg<false, false, 256, 5, true, true>(args.qcodes, w, args, num_sms, s, why);
 }
+
+int set_pair_limit(int pairs) { return g_pair_limit.exchange(pairs < 0 ? 0 : pairs); }
 
 cudaError_t watchdog_read(uint32_t* value, bool clear) {
   cudaError_t e = cudaMemcpyFromSymbol(value, g_watchdog, sizeof(uint32_t));

@@ -86,6 +86,10 @@ cudaError_t launch_rope_kv_insert(const void* q, void* q_out, int64_t T, int H, 
                                   const float* scale, int32_t* err_flag, int num_sms,
                                   cudaStream_t s);
 
+// Caps the CTA pairs of the pair-form GEMM launches (0 = no cap); returns
+// the previous cap.
+int set_pair_limit(int pairs);
+
 cudaError_t watchdog_read(uint32_t* value, bool clear);
 
 // One tiny kernel whose only wait can never be satisfied; it must give up

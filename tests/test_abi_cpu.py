@@ -231,3 +231,9 @@ def test_rope_kv_insert_argument_errors(L):
 def test_rope_kv_insert_valid_call_without_device(L):
     assert kv_insert(L) == 7
     assert kv_insert(L, q_out=P) == 7  # in place
+
+
+def test_pair_limit_is_a_plain_setting(L):
+    assert L.mxq_debug_set_pair_limit(5) == 0
+    assert L.mxq_debug_set_pair_limit(-3) == 5
+    assert L.mxq_debug_set_pair_limit(0) == 0

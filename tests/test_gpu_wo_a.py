@@ -251,3 +251,29 @@ def test_maximum_d(mxq, T):
     out, _ = run(mxq, x, pos, cos, sin, w, sw, 64)
     a, sa = oracle_quant(x, pos, cos, sin, 64)
     check_gemm(out, *O.bmm_a8w8_ref(a, sa, w, sw), f"D=65536 T={T}")
+
+
+@pytest.mark.parametrize("pairs", [1, 7, 30])
+def test_pair_forms_with_fewer_pairs_than_slots(mxq, pairs):
+    """The many-token launches with their grid capped below the device's
+    cluster slots (a host-side launch parameter): every pair then walks more
+    units and the quantising launch deals its jobs over fewer pairs; no wait
+    may run out (the fixture checks the watchdog) and the outputs must be
+    bit-identical to the uncapped quantiser + GEMM."""
+    T, G, D, N = 1100, 8, 4096, 1024
+    x, pos, cos, sin = wo_a_inputs(T, G, D, N, 64, seed=2300, pos_mode="arange")
+    w, sw = oracle_weights(G, N, D, seed=3)
+    xd, pd, cd, sd, wd, swd = to_dev(x, pos, cos, sin, w, sw)
+    wsf = mxq.mxq_prepare_weight_scales(swd, D)
+    q, sc = mxq.mxq_inv_rope_group_quant(xd, pd, cd, sd, 64)
+    ref = mxq.mxq_bmm_a8w8(q, sc, wd, wsf)
+    torch.cuda.synchronize()
+    prev = mxq.mxq_debug_set_pair_limit(pairs)
+    try:
+        out = mxq.mxq_wo_a(xd, pd, cd, sd, wd, wsf, R=64)
+        gemm = mxq.mxq_bmm_a8w8(q, sc, wd, wsf)
+        torch.cuda.synchronize()
+    finally:
+        mxq.mxq_debug_set_pair_limit(prev)
+    assert torch.equal(out, ref)
+    assert torch.equal(gemm, ref)
