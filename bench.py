@@ -550,8 +550,9 @@ def run_reference(args, rank):
 
 
 def single_workload(mxq, device, peaks, args):
-    """Eager run of one secondary workload (decode layer or MXFP8 linear) over
-    24 distinct weight sets: --warmup passes, then --steps timed calls."""
+    """Eager run of one secondary workload (decode layer or MXFP8 linear over 24
+    distinct weight sets, or the KV insert over 4 caches): --warmup passes,
+    then --steps timed calls."""
     import workloads as W
 
     n_sets = 24
@@ -571,6 +572,22 @@ def single_workload(mxq, device, peaks, args):
 
         byt = G * N * D + G * N * KG + T * (2 * G * D + 8 + 2 * (R // 2) * 2) + 2 * T * G * N
         desc = f"wo_a decode x [{T},8,4096] -> [{T},8,1024], W [8,1024,4096], {n_sets} weight sets"
+    elif args.workload == "kv":
+        T, Hq, Dh, Rk = args.tokens, 64, 512, 64
+        q = W.bf16_normal_cuda((T, Hq, Dh), seed=8100, device=device)
+        kv = W.bf16_normal_cuda((T, Dh), seed=8101, std=4.0, device=device)
+        pos = torch.arange(32768, 32768 + T, dtype=torch.int64, device=device)
+        cos, sin = rope_tables(32768 + T, device)
+        slots = torch.randperm(4 * T, device=device)[:T].to(torch.int64)
+        caches = [torch.zeros((4 * T, Dh), dtype=torch.uint8, device=device) for _ in range(4)]
+        scale = torch.tensor([0.0371], dtype=torch.float32, device=device)
+        q_out = torch.empty_like(q)
+
+        def call(i):
+            mxq.mxq_rope_kv_insert(q, kv, pos, cos, sin, Rk, slots, caches[i % 4], scale=scale, q_out=q_out)
+
+        byt = 2 * (2 * T * Hq * Dh) + T * (2 * Dh + Dh + 8 + 8 + 2 * Rk)
+        desc = f"forward RoPE + E4M3 KV insert, q [{T},64,512] out of place, kv [{T},512]"
     else:
         M, K, Nl = args.tokens, args.k, W.LINEAR_N
         kg = (K + 127) // 128
@@ -616,10 +633,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--workload", choices=["prefill", "decode", "linear"], default="prefill",
-                    help="prefill (default, the headline); decode / linear: a short eager run "
+    ap.add_argument("--workload", choices=["prefill", "decode", "linear", "kv"], default="prefill",
+                    help="prefill (default, the headline); decode / linear / kv: a short eager run "
                          "of that workload alone (for profiling), its own JSON line")
-    ap.add_argument("--tokens", type=int, default=1, help="T (decode) or M (linear)")
+    ap.add_argument("--tokens", type=int, default=1, help="T (decode, kv) or M (linear)")
     ap.add_argument("--k", type=int, default=576, help="K of the linear workload")
     args = ap.parse_args()
 

@@ -323,18 +323,27 @@ int mxq_linear_noalloc(const void* x_bf16, const uint8_t* w_e4m3, const uint8_t*
                        void* out_bf16, int64_t M, int32_t N, int32_t K, mxq_stream_t stream);
 
 /*
- * Testing aid (the pages have no counterpart): caps the number of CTA pairs
- * that the many-token GEMM forms launch -- mxq_bmm_a8w8, mxq_wo_a and
- * mxq_linear above 128 tokens -- for the whole process; 0 (the default)
- * launches one pair per cluster slot that fits on the device.  Results do
- * not depend on the cap: every pair walks the work units with a stride of
- * the pair count, and the one-launch prefill deals its quantisation jobs by
- * unit, so any grid covers all of them.  That launch is cooperative: all its
- * pairs are resident together (they wait on each other's job counters), so
- * a grid that cannot fit is refused rather than left waiting.  Returns the
- * previous cap; a negative value is taken as 0.
+ * Testing aids (the pages have no counterpart), process-wide settings that
+ * change no result.
+ *
+ * mxq_debug_set_pair_limit caps the number of CTA pairs that the many-token
+ * GEMM forms launch -- mxq_bmm_a8w8, mxq_wo_a and mxq_linear above 128
+ * tokens; 0 (the default) launches one pair per cluster slot that fits on
+ * the device.  Every pair walks the work units with a stride of the pair
+ * count, and the one-launch prefill deals its quantisation jobs by unit, so
+ * any grid covers all of them.  Returns the previous cap (a negative value
+ * is taken as 0).
+ *
+ * mxq_debug_set_lazy_pairs makes the pairs of the one-launch prefill from
+ * index `from` on skip the quantisation jobs they own, as if they had not
+ * started (a negative value, the default: none).  A pair that waits on a job
+ * for more than 50 us quantises it itself, so a pair that is not running --
+ * for example while a kernel of another stream holds SMs -- delays the
+ * others instead of stalling them; this setting exercises that path.
+ * Returns the previous setting.
  */
 int mxq_debug_set_pair_limit(int pairs);
+int mxq_debug_set_lazy_pairs(int from);
 
 /*
  * Watchdog word of the GEMM kernels on the current device (host call,

@@ -422,6 +422,11 @@ int mxq_rope_kv_insert(const void* q_bf16, void* q_out_bf16, int64_t T, int32_t 
 
 int mxq_debug_set_pair_limit(int pairs) { return mxq::set_pair_limit(pairs); }
 
+int mxq_debug_set_lazy_pairs(int from) {
+  const int prev = mxq::set_lazy_pairs(from);
+  return prev >= (1 << 30) ? -1 : prev;
+}
+
 int mxq_watchdog_read(uint32_t* host_value, int clear) {
   if (!host_value) return fail(MXQ_ERR_NULL, "host_value is NULL");
   int sms = 0;

@@ -92,6 +92,9 @@ __device__ uint32_t g_watchdog;
 // Cap on the CTA pairs of the pair forms (0: one pair per co-resident
 // cluster slot); a testing aid, see mxq_debug_set_pair_limit.
 std::atomic<int> g_pair_limit{0};
+// Testing aid, see mxq_debug_set_lazy_pairs: pairs from this index on skip
+// their quantisation jobs (as if they never started).
+std::atomic<int> g_lazy_from{1 << 30};
 
 namespace {
 
@@ -126,6 +129,10 @@ constexpr int kQPrefetch = 2;
 // else ready): the gpu-scope fence waits for every store the warp still has
 // in flight.
 constexpr int kQPublish = 4;
+// A job that a consumer has waited on this long is quantised by the
+// consumer itself (its owner may not be running, e.g. while a kernel of
+// another stream holds SMs); in normal operation no wait comes near it.
+constexpr uint64_t kTakeoverNs = 50000;
 
 struct BmmArgs {
   const uint8_t* a_sf;  // [T][G][KG]
@@ -150,6 +157,7 @@ struct BmmArgs {
   uint8_t* qatoms;     // [G][MB][KG][512] activation scale atoms
   uint32_t* qflags;    // [G][MB][KG] job counters, zero before the launch
   int MB;              // 128-token blocks per group (2 * x_tiles)
+  int q_lazy_from;     // testing aid: pairs from this index on quantise nothing
 };
 
 // PAIR: the CTA-pair form (normal orientation only): MMA M = 256 tokens, 128
@@ -194,10 +202,15 @@ struct Cfg {
   // Quantising form: the BF16 activation slices.
   static constexpr int QX_BYTES = QUANT ? kQSlots * kQSliceBytes : 0;
   static constexpr int OFF_QX = OFF_OUT + OUT_BYTES;
-  static constexpr int OFF_BAR = OFF_QX + QX_BYTES;
+  // Quantising form: the activation producer's slot for quantising a job
+  // whose owner is late (one slice at a time).
+  static constexpr int TK_BYTES = QUANT ? kQSliceBytes : 0;
+  static constexpr int OFF_TK = OFF_QX + QX_BYTES;
+  static constexpr int OFF_BAR = OFF_TK + TK_BYTES;
   // full[NSTAGE], empty[NSTAGE], landed[NSTAGE], acc_full, acc_empty,
-  // sf_full[2], sf_empty[2], mma_done, then qfull[kQSlots]
-  static constexpr int N_BARS = 3 * NSTAGE + 7 + (QUANT ? kQSlots : 0);
+  // sf_full[2], sf_empty[2], mma_done, then qfull[kQSlots] and the takeover
+  // slot's barrier
+  static constexpr int N_BARS = 3 * NSTAGE + 7 + (QUANT ? kQSlots + 1 : 0);
   static constexpr int OFF_SLOT = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_SLOT + 16 + 1024;
   // Two CTAs share an SM when their shared memory allows it (the small-token
@@ -463,6 +476,87 @@ __device__ __forceinline__ void qslice_plain(const BmmArgs& p, const QJob& j, in
   }
 }
 
+// Quantises job (g, 128-token block starting at t0, K group kg), counter f,
+// in the calling warp, one 16-row slice at a time through the warp's own
+// slot `tslot` (barrier `tbar`, whose phase bit `tphase` it advances), and
+// raises the counter by kQSlices.  Used by a consumer whose wait on the
+// job's owner ran long.  Lane r < 16 does row r of each slice on its own, in
+// two passes over the slot (group abs-max, then codes), with the helpers and
+// the order of operations of the epilogue warps, so the bytes are the same;
+// the owner may still quantise the same job (both write the same bytes, and
+// a counter above kQSlices reads as complete).  Written for few live
+// registers: it sits in the kernel's rarely taken path, and a larger
+// footprint there would cost the whole kernel registers.  Returns false when
+// a copy did not land in time.
+__device__ __forceinline__ bool take_over_job(const BmmArgs& p, const CUtensorMap* xq,
+                                              uint8_t* tslot, uint64_t* tbar, uint32_t& tphase,
+                                              int g, int kg, int t0, int f, int lane) {
+  const bool rope = p.R > 0 && kg == p.KG - 1;
+  const int first = 16 - (p.R >> 3);  // first chunk of the rotated slice
+  const int dist = p.R >> 4;          // chunks between rotate-half partners
+  for (int sl = 0; sl < kQSlices; ++sl) {
+    ptx::fence_proxy_async_smem();  // the slot's previous contents were read
+    __syncwarp();
+    if (lane == 0) {
+      ptx::mbar_arrive_expect_tx(tbar, kQSliceBytes);
+      ptx::tma_load_3d(tslot, xq, tbar, kg * 128, g, t0 + kQRows * sl);
+    }
+    const bool landed_ok = ptx::mbar_wait(tbar, tphase, kWaitLimitNs);
+    tphase ^= 1u;
+    if (!__all_sync(0xffffffffu, landed_ok)) return false;
+    if (lane < kQRows) {
+      const int rr = kQRows * sl + lane;  // row within the 128-token block
+      const int t = t0 + rr;
+      const bool valid = t < p.T;
+      const int64_t pl = (p.R > 0 && valid) ? __ldg(p.pos + t) : 0;
+      const bool bad = p.R > 0 && valid && (pl < 0 || pl >= p.max_pos);
+      const uint8_t* row = tslot + lane * 256;
+      // The fp32 values of chunk c (8 elements), rotated when c lies in the
+      // slice: inverse RoPE against the partner chunk R/16 chunks away, with
+      // the cos/sin entries both halves of a pair share.
+      auto chunk = [&](int c, float (&y)[8]) {
+        unpack8(*reinterpret_cast<const uint4*>(row + c * 16), y);
+        if (rope && c >= first && valid && !bad) {
+          const bool lower = c < first + dist;
+          float xp[8];
+          unpack8(*reinterpret_cast<const uint4*>(row + (lower ? c + dist : c - dist) * 16), xp);
+          const int i0 = (c - first - (lower ? 0 : dist)) * 8;
+          const uint4 cw = __ldg(reinterpret_cast<const uint4*>(p.cos_tab + pl * p.cs_ld + i0));
+          const uint4 sw = __ldg(reinterpret_cast<const uint4*>(p.sin_tab + pl * p.cs_ld + i0));
+          inv_rope8(y, xp, cw, sw, lower);
+        }
+      };
+      float amax = 0.0f;
+      for (int c = 0; c < 16; ++c) {
+        float y[8];
+        chunk(c, y);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(y[e]));
+      }
+      uint32_t sb = 0;
+      for (int c = 0; c < 16; ++c) {
+        float y[8];
+        chunk(c, y);
+        uint2 q8 = encode8(y, amax, &sb);
+        if (bad) q8 = make_uint2(0, 0);
+        const int col = kg * 128 + c * 8;
+        if (valid && col < p.K)
+          *reinterpret_cast<uint2*>(p.qcodes + ((size_t)t * p.G + g) * p.K + col) = q8;
+      }
+      *reinterpret_cast<uint32_t*>(p.qatoms + (size_t)f * kSfAtomBytes + (rr % 32) * 16 +
+                                   (rr / 32) * 4) = (valid ? (bad ? 0u : sb) : 127u) * 0x01010101u;
+      if (bad && kg == 0 && p.err_flag != nullptr) atomicOr(p.err_flag, MXQ_DEVERR_POSITION);
+    }
+  }
+  // Publish as the epilogue warps do: the codes and atom words are read by
+  // other CTAs through TMA.
+  ptx::fence_proxy_async_global();
+  ptx::fence_acq_rel_gpu();
+  __syncwarp();
+  if (lane == 0) ptx::red_add_relaxed_gpu(p.qflags + f, (uint32_t)kQSlices);
+  return true;
+}
+
 // Tensor maps only the quantising form takes (the activation scale atoms it
 // writes and its BF16 input); the other forms take an empty parameter, so
 // that their launches copy no more parameter bytes than they use.
@@ -538,7 +632,7 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
     }
     ptx::mbar_init(mma_done, 1);
     if (QUANT)
-      for (int i = 0; i < kQSlots; ++i) ptx::mbar_init(&qfull[i], 1);
+      for (int i = 0; i < kQSlots + 1; ++i) ptx::mbar_init(&qfull[i], 1);
     abort_shared = 0;
     ptx::fence_barrier_init();
   }
@@ -722,6 +816,9 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
     // both counted on the even CTA's stage barrier.
     int it = 0;
     bool stop = false;
+    uint8_t* tslot = smem + C::OFF_TK;
+    uint64_t* tbar = qfull + kQSlots;
+    uint32_t tphase = 0;
     ptx::griddep_wait();
     for (int u = u_first; u < p.units && !stop; u += u_step) {
       const Unit w = decode_unit<SWAP, BN>(p, u);
@@ -749,7 +846,8 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
             const uint32_t mask = __ballot_sync(0xffffffffu, rdy);
             nready = mask == 0xffffffffu ? 32 : __ffs(~mask) - 1;  // ready stages in a row
             if (nready > 0) break;
-            int give_up = 0;  // 1: another role aborted, 2: this wait ran out
+            // 1: another role aborted, 2: this wait ran out, 3: take the job over
+            int give_up = 0;
             if (lane == 0) {
               const uint64_t now = ptx::globaltimer();
               if (*abort_flag)
@@ -758,8 +856,21 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
                 t0 = now;
               else if (now - t0 > kWaitLimitNs)
                 give_up = 2;
+              else if (now - t0 > kTakeoverNs)
+                give_up = 3;
             }
             give_up = __shfl_sync(0xffffffffu, give_up, 0);
+            if (give_up == 3) {
+              // The first stage not ready (stage kk): quantise its job here.
+              if (!take_over_job(p, map_xq(qmaps), tslot, tbar, tphase, w.g, w.kg_begin + kk,
+                                 (w.x0 / 128 + (int)rank) * 128, fbase + kk, lane)) {
+                if (lane == 0) watchdog(abort_flag, kWdProducer);
+                stop = true;
+                break;
+              }
+              t0 = 0;
+              continue;
+            }
             if (give_up) {
               if (give_up == 2 && lane == 0) watchdog(abort_flag, kWdProducer);
               stop = true;
@@ -1108,7 +1219,7 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
       uint8_t* qslot = smem + C::OFF_QX + qw * kQSliceBytes;
       uint64_t* qbar = &qfull[qw];
       QJob j;
-      bool have = qjob_first(p, u_first, u_step, (int)rank, j);
+      bool have = u_first < p.q_lazy_from && qjob_first(p, u_first, u_step, (int)rank, j);
       int k = 0, npend = 0;  // slices copied into the slot; counters not yet raised
       int pend[kQPublish];
       auto pos_of = [&](const QJob& jj) -> int64_t {
@@ -1623,7 +1734,7 @@ cudaError_t launch_cfg(const void* a, const uint8_t* w, BmmArgs args, int num_sm
   // Programmatic dependent launch: the grid may start while the preceding
   // kernel on the stream finishes; it waits (griddepcontrol.wait) before
   // reading anything that kernel produced.
-  cudaLaunchAttribute attr[3];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
@@ -1636,18 +1747,7 @@ cudaError_t launch_cfg(const void* a, const uint8_t* w, BmmArgs args, int num_sm
     attr[cfg.numAttrs].val.clusterDim.z = 1;
     ++cfg.numAttrs;
   }
-  if (QUANT) {
-    // The quantising pairs wait on job counters that other pairs raise, so
-    // every pair of the grid must be resident at the same time.  A
-    // cooperative launch guarantees that: the grid starts only once all of
-    // it fits beside whatever else runs on the device (a kernel of another
-    // stream holding SMs delays the start instead of stranding pairs that
-    // wait on pairs that cannot start), and a grid that can never fit is
-    // refused at launch.
-    attr[cfg.numAttrs].id = cudaLaunchAttributeCooperative;
-    attr[cfg.numAttrs].val.cooperative = 1;
-    ++cfg.numAttrs;
-  }
+
   int grid = args.units;
   if (PAIR) {
     // One persistent CTA pair per co-resident cluster slot (the SM pairs the
@@ -1768,6 +1868,7 @@ cudaError_t launch_wo_a_prefill(const void* x, const int64_t* pos, const void* c
   args.splits = 1;
   args.kg_per_split = args.KG;
   args.MB = 2 * args.x_tiles;
+  args.q_lazy_from = g_lazy_from.load(std::memory_order_relaxed);
   const WoaPrefillLayout l = woa_prefill_layout(T, G, K);
   uint8_t* base = static_cast<uint8_t*>(ws);
   args.xq = reinterpret_cast<const uint16_t*>(x);
@@ -1782,6 +1883,7 @@ cudaError_t launch_wo_a_prefill(const void* x, const int64_t* pos, const void* c
 }
 
 int set_pair_limit(int pairs) { return g_pair_limit.exchange(pairs < 0 ? 0 : pairs); }
+int set_lazy_pairs(int from) { return g_lazy_from.exchange(from < 0 ? (1 << 30) : from); }
 
 cudaError_t watchdog_read(uint32_t* value, bool clear) {
   cudaError_t e = cudaMemcpyFromSymbol(value, g_watchdog, sizeof(uint32_t));

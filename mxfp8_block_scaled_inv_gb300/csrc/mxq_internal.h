@@ -89,6 +89,9 @@ cudaError_t launch_rope_kv_insert(const void* q, void* q_out, int64_t T, int H, 
 // Caps the CTA pairs of the pair-form GEMM launches (0 = no cap); returns
 // the previous cap.
 int set_pair_limit(int pairs);
+// Pairs of the quantising form from this index on skip their quantisation
+// jobs (a negative value: none); returns the previous setting.
+int set_lazy_pairs(int from);
 
 cudaError_t watchdog_read(uint32_t* value, bool clear);
 

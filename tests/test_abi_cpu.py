@@ -237,3 +237,9 @@ def test_pair_limit_is_a_plain_setting(L):
     assert L.mxq_debug_set_pair_limit(5) == 0
     assert L.mxq_debug_set_pair_limit(-3) == 5
     assert L.mxq_debug_set_pair_limit(0) == 0
+
+
+def test_lazy_pairs_is_a_plain_setting(L):
+    assert L.mxq_debug_set_lazy_pairs(3) == -1
+    assert L.mxq_debug_set_lazy_pairs(-1) == 3
+    assert L.mxq_debug_set_lazy_pairs(-5) == -1

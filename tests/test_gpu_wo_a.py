@@ -277,3 +277,32 @@ def test_pair_forms_with_fewer_pairs_than_slots(mxq, pairs):
         mxq.mxq_debug_set_pair_limit(prev)
     assert torch.equal(out, ref)
     assert torch.equal(gemm, ref)
+
+
+@pytest.mark.parametrize("lazy_from", [0, 5, 40])
+def test_pair_quant_when_owners_do_not_quantise(mxq, lazy_from):
+    """Pairs of the one-launch prefill from index `lazy_from` on skip the
+    quantisation jobs they own, as if they never ran (0: no pair quantises
+    anything).  The pairs waiting on those jobs must quantise them
+    themselves after their takeover wait -- several consumers may do the
+    same job, writing the same bytes -- with no wait running out (the
+    fixture checks the watchdog), and the output must be bit-identical to
+    quantiser + GEMM."""
+    T, G, D, N = 1100, 8, 4096, 1024
+    x, pos, cos, sin = wo_a_inputs(T, G, D, N, 64, seed=2400, pos_mode="arange")
+    w, sw = oracle_weights(G, N, D, seed=3)
+    xd, pd, cd, sd, wd, swd = to_dev(x, pos, cos, sin, w, sw)
+    wsf = mxq.mxq_prepare_weight_scales(swd, D)
+    q, sc = mxq.mxq_inv_rope_group_quant(xd, pd, cd, sd, 64)
+    ref = mxq.mxq_bmm_a8w8(q, sc, wd, wsf)
+    ws = torch.full((mxq.mxq_wo_a_workspace_bytes(T, G, D, N),), 0xA5, dtype=torch.uint8,
+                    device="cuda")
+    torch.cuda.synchronize()
+    prev = mxq.mxq_debug_set_lazy_pairs(lazy_from)
+    try:
+        out = mxq.mxq_wo_a(xd, pd, cd, sd, wd, wsf, R=64, ws=ws)
+        torch.cuda.synchronize()
+    finally:
+        mxq.mxq_debug_set_lazy_pairs(prev)
+    assert torch.equal(out, ref)
+    assert np.array_equal(ws[:T * G * D].cpu().numpy().reshape(T, G, D), q.cpu().numpy())
