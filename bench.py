@@ -338,6 +338,7 @@ def kv_insert_bench(mxq, device, peaks):
         us = a.elapsed_time(b) * 1e3 / reps
         out[name] = {"us": round(us, 2), "algorithmic_bytes": byt, "gbs": round(byt / (us * 1e-6) / 1e9, 1),
                      "hbm_frac": round(byt / (us * 1e-6) / 1e9 / hbm, 3)}
+    out["prefill_out_of_place"]["traffic"] = measured_traffic("rope_kv_insert_prefill_8k")
     del q, kv, q_out, cache
     torch.cuda.empty_cache()
     dec = {}
