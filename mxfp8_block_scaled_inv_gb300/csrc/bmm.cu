@@ -1802,7 +1802,7 @@ cudaError_t launch_bmm_a8w8(const uint8_t* a, const uint8_t* a_sf, const uint8_t
     args.y_tiles = 1;
     if (T <= 16) return launch_cfg<true, false, 16, 5>(a, w, args, num_sms, s, why);
     if (T <= 32) return launch_cfg<true, false, 32, 4>(a, w, args, num_sms, s, why);
-    if (T <= 64) return launch_cfg<true, false, 64, 6>(a, w, args, num_sms, s, why);
+    if (T <= 64) return launch_cfg<true, false, 64, 4>(a, w, args, num_sms, s, why);
     return launch_cfg<true, false, 128, 4>(a, w, args, num_sms, s, why);
   }
   // Many tokens: CTA pairs, 256 tokens x 256 weight rows per unit.
