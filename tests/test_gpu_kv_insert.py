@@ -175,3 +175,24 @@ def test_prefill_chunk(mxq):
                                  W.bf16_bits(cos), W.bf16_bits(sin), R, -np.ones(len(idx), np.int64),
                                  np.zeros((1, D), dtype=np.uint8), scale=0.0371)
     assert np.array_equal(W.bf16_bits(q_out[idx].cpu()), want_q)
+
+
+def test_strided_cos_sin_views(mxq):
+    """cos/sin as column slices of a wider cache (row stride 48 > R/2 = 32):
+    only the first R/2 entries of each row are used."""
+    T, H, D, R = 16, 4, 256, 64
+    q, kv, pos, _, _, slots, ns = inputs(T, H, D, D, R, seed=5600, max_pos=300)
+    cw, swide = W.rope_cache(300, 96)  # 48 entries per row
+    cos, sin = cw[:, :32], swide[:, :32]
+    qd, kvd, pd = to_dev(q, kv, pos)
+    cdw, sdw = to_dev(cw, swide)
+    cache = torch.full((ns, D), 0xA5, dtype=torch.uint8, device="cuda")
+    sc = torch.tensor([0.0371], dtype=torch.float32, device="cuda")
+    q_out = mxq.mxq_rope_kv_insert(qd, kvd, pd, cdw[:, :32], sdw[:, :32], R,
+                                   torch.from_numpy(slots).cuda(), cache, scale=sc)
+    torch.cuda.synchronize()
+    want_q, want_cache = O.rope_kv_insert(W.bf16_bits(q), W.bf16_bits(kv), pos.numpy(),
+                                          W.bf16_bits(cos.contiguous()), W.bf16_bits(sin.contiguous()), R,
+                                          slots, np.full((ns, D), 0xA5, dtype=np.uint8), scale=0.0371)
+    assert np.array_equal(W.bf16_bits(q_out.cpu()), want_q)
+    assert np.array_equal(cache.cpu().numpy(), want_cache)

@@ -306,3 +306,28 @@ def test_pair_quant_when_owners_do_not_quantise(mxq, lazy_from):
         mxq.mxq_debug_set_lazy_pairs(prev)
     assert torch.equal(out, ref)
     assert np.array_equal(ws[:T * G * D].cpu().numpy().reshape(T, G, D), q.cpu().numpy())
+
+
+def test_pair_quant_takeover_with_invalid_positions(mxq):
+    """Every job quantised by its consumers (no pair quantises its own), with
+    some positions outside the table: those tokens' outputs are zero and the
+    error bit is set, every other token as the oracle."""
+    T, G, D, N = 300, 2, 512, 256
+    x, _, cos, sin = wo_a_inputs(T, G, D, N, 64, seed=2500, max_pos=100, max_pos_table=100)
+    rng = np.random.Generator(np.random.PCG64(2501))
+    pos = torch.from_numpy(rng.integers(0, 100, T).astype(np.int64))
+    bad = np.array([0, 17, 130, 255, 299])
+    pos[bad] = torch.tensor([-1, 100, 1000, -7, 100], dtype=torch.int64)
+    w, sw = oracle_weights(G, N, D, seed=2502)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    prev = mxq.mxq_debug_set_lazy_pairs(0)
+    try:
+        out, _ = run(mxq, x, pos, cos, sin, w, sw, 64, err=err)
+    finally:
+        mxq.mxq_debug_set_lazy_pairs(prev)
+    assert int(err.item()) == mxq.MXQ_DEVERR_POSITION
+    o = out.float().cpu()
+    assert (o[bad] == 0).all()
+    good = np.setdiff1d(np.arange(T), bad)
+    a, sa = oracle_quant(x[good], pos[good], cos, sin, 64)
+    check_gemm(out[good], *O.bmm_a8w8_ref(a, sa, w, sw), "good rows, jobs taken over")
