@@ -67,7 +67,9 @@
 //           TMA-loads the codes and atoms as soon as they are published.  The
 //           quantising work waits only for its own copies, so the counters
 //           always complete (every CTA of the persistent grid is resident).
-//           (warp 2, the scale loader in the other pair form, is idle.)
+//           This form has no scale loader: its gate runs on warp 2 and the
+//           CTA has 12 warps, which leaves 168 registers per thread (three
+//           warps per SM sub-partition instead of four).
 // Every wait is bounded in wall time; on expiry the kernel sets a watchdog
 // bit, stops issuing, drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -108,6 +110,7 @@ constexpr int kEpiWarp0 = 3;   // epilogue warps 3-10
 constexpr int kEpiWarps = 8;
 constexpr int kActWarp = 11;   // activation producer (unfused forms)
 constexpr int kGateWarp = 12;  // pair form: waits on the MMA warp's barriers
+constexpr int kQGateWarp = 2;  // the same role in the quantising pair form
 // Quantising pair form: a job (128 rows of one K group) is kQSlices slices
 // of 16 rows x 128 values, and epilogue warp w quantises slice w of every
 // job of its CTA, between accumulator drains, from its own shared-memory slot
@@ -229,8 +232,9 @@ struct Cfg {
   // producer warp.
   // The pair form adds a gate warp that does the MMA warp's barrier waits:
   // the tensor pipe's instruction queue is shallow, so any wait in the
-  // issuing warp between stages leaves the pipe idle.
-  static constexpr int THREADS = (FUSED ? 11 : (PAIR ? 13 : 12)) * 32;
+  // issuing warp between stages leaves the pipe idle.  The quantising pair
+  // form needs no scale loader and runs its gate on that warp.
+  static constexpr int THREADS = (FUSED ? 11 : (PAIR && !QUANT ? 13 : 12)) * 32;
   // Instruction descriptor, kind::mxf8f6f4 with block scaling: E4M3 A and
   // B (format 0), both K-major, N >> 3 at bits 17-22, UE8M0 scale type at
   // bit 23, M >> 4 at bits 24-28, scale-factor ids 0.
@@ -1054,7 +1058,7 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
     }
     __syncwarp();
     if (!ptx::mbar_wait(mma_done, 0, kWaitLimitNs)) watchdog(abort_flag, kWdDrain);
-  } else if (warp == 2) {
+  } else if (warp == 2 && !QUANT) {
     // ------------------------------------------------- activation scales
     // (The fused and quantising forms need no loader.)
     if constexpr (!FUSED && !QUANT) {
@@ -1107,7 +1111,7 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
       }
     }
     }
-  } else if (warp == kGateWarp) {
+  } else if (warp == (QUANT ? kQGateWarp : kGateWarp)) {
     // ---------------------------------------------------- gate (pair form)
     // Waits, for the even CTA's MMA warp, on the accumulator at each unit's
     // start and on each stage's full barrier, then meets the MMA warp at a
@@ -1178,8 +1182,8 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
       // which never drain this way.)
       auto pair_drain = [&](const Unit& w) {
         // Drain 32 columns at a time and keep them as packed BF16 pairs (RNE,
-        // as in the other forms), so that the 13-warp CTA fits its register
-        // budget; the accumulator is released as soon as it is read.
+        // as in the other forms), so that the CTA fits its register budget;
+        // the accumulator is released as soon as it is read.
         uint32_t pk[C::HALF / 2];
   #pragma unroll
         for (int c = 0; c < C::HALF / 32; ++c) {
