@@ -341,9 +341,16 @@ int mxq_linear_noalloc(const void* x_bf16, const uint8_t* w_e4m3, const uint8_t*
  * for example while a kernel of another stream holds SMs -- delays the
  * others instead of stalling them; this setting exercises that path.
  * Returns the previous setting.
+ *
+ * mxq_debug_takeovers writes to *host_value how many quantisation jobs of
+ * the one-launch prefill on the current device were quantised by a waiting
+ * pair instead of their owner since the last clear (host call, synchronous;
+ * with clear != 0 the count is reset after reading).  0 after a call means
+ * no pair ever waited 50 us for a job.  MXQ_ERR_NULL for a NULL host_value.
  */
 int mxq_debug_set_pair_limit(int pairs);
 int mxq_debug_set_lazy_pairs(int from);
+int mxq_debug_takeovers(uint32_t* host_value, int clear);
 
 /*
  * Watchdog word of the GEMM kernels on the current device (host call,

@@ -23,7 +23,7 @@ __all__ = [
     "mxq_dequant_bf16", "mxq_scales_f32_to_e8m0", "mxq_watchdog_read", "mxq_watchdog_selftest",
     "mxq_arch_supported",
     "mxq_version", "mxq_wo_a_workspace_bytes", "mxq_wo_a", "wo_a", "mxq_rope_kv_insert",
-    "mxq_debug_set_pair_limit", "mxq_debug_set_lazy_pairs",
+    "mxq_debug_set_pair_limit", "mxq_debug_set_lazy_pairs", "mxq_debug_takeovers",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -72,6 +72,7 @@ _SIGNATURES = {
     "mxq_watchdog_selftest": (ctypes.c_int, [ctypes.c_uint64, _vp]),
     "mxq_debug_set_pair_limit": (ctypes.c_int, [ctypes.c_int]),
     "mxq_debug_set_lazy_pairs": (ctypes.c_int, [ctypes.c_int]),
+    "mxq_debug_takeovers": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "mxq_wo_a_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32]),
     "mxq_rope_kv_insert": (ctypes.c_int, [_vp, _vp, _i64, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _i64,
                                           _i64, _i32, _vp, _vp, _i64, _i32, _vp, _vp, _vp]),
@@ -263,6 +264,14 @@ def mxq_debug_set_lazy_pairs(first):
     """Testing aid: pairs of the one-launch prefill from index `first` on skip
     their quantisation jobs (negative: none); returns the previous setting."""
     return lib().mxq_debug_set_lazy_pairs(int(first))
+
+
+def mxq_debug_takeovers(clear=False):
+    """Testing aid: prefill quantisation jobs quantised by a waiting pair
+    instead of their owner since the last clear."""
+    v = ctypes.c_uint32(0)
+    _check("mxq_debug_takeovers", lib().mxq_debug_takeovers(ctypes.byref(v), 1 if clear else 0))
+    return v.value
 
 
 def mxq_watchdog_selftest(limit_ns=1_000_000, stream=None):

@@ -427,6 +427,13 @@ int mxq_debug_set_lazy_pairs(int from) {
   return prev >= (1 << 30) ? -1 : prev;
 }
 
+int mxq_debug_takeovers(uint32_t* host_value, int clear) {
+  if (!host_value) return fail(MXQ_ERR_NULL, "host_value is NULL");
+  int sms = 0;
+  if (int st = device_check(&sms)) return st;
+  return cuda_status(mxq::takeover_count(host_value, clear != 0), "takeover count read");
+}
+
 int mxq_watchdog_read(uint32_t* host_value, int clear) {
   if (!host_value) return fail(MXQ_ERR_NULL, "host_value is NULL");
   int sms = 0;

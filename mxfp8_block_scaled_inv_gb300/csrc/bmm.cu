@@ -90,6 +90,8 @@
 namespace mxq {
 
 __device__ uint32_t g_watchdog;
+// Jobs of the one-launch prefill quantised by a consumer (a testing aid).
+__device__ uint32_t g_takeovers;
 
 // Cap on the CTA pairs of the pair forms (0: one pair per co-resident
 // cluster slot); a testing aid, see mxq_debug_set_pair_limit.
@@ -128,6 +130,8 @@ constexpr uint32_t kEpiPollNs = 32;
 // Each quantising warp prefetches its slice of the job this many jobs ahead
 // into L2 (its shared-memory copies then wait on L2, not DRAM).
 constexpr int kQPrefetch = 2;
+// Quantisation runs at most this many units ahead of the CTA's GEMM.
+constexpr int kQLead = 1;
 // Publications are batched (and made at once whenever the warp has nothing
 // else ready): the gpu-scope fence waits for every store the warp still has
 // in flight.
@@ -872,6 +876,7 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
                 stop = true;
                 break;
               }
+              if (lane == 0) atomicAdd(&g_takeovers, 1u);
               t0 = 0;
               continue;
             }
@@ -1221,6 +1226,16 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
         }
       };
       uint8_t* qslot = smem + C::OFF_QX + qw * kQSliceBytes;
+      // x is read once: its lines leave L2 first, ahead of the codes, which
+      // the CTA pairs read back shortly after.
+      const uint64_t x_policy = ptx::policy_evict_first();
+      // The y_tiles units of a token block share its jobs and are
+      // consecutive, so their ordinals (in their pairs) differ by at most
+      // ceil((y_tiles - 1) / u_step).  With a lead of at least that, the
+      // jobs that the pair furthest behind is multiplying are always
+      // allowed, wherever they fall: the pairs cannot wait on each other in
+      // a cycle.
+      const int q_lead = max(kQLead, (p.y_tiles - 1 + u_step - 1) / u_step);
       uint64_t* qbar = &qfull[qw];
       QJob j;
       bool have = u_first < p.q_lazy_from && qjob_first(p, u_first, u_step, (int)rank, j);
@@ -1233,7 +1248,8 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
       auto load_slice = [&](const QJob& jj) {
         if (lane == 0) {
           ptx::mbar_arrive_expect_tx(qbar, kQSliceBytes);
-          ptx::tma_load_3d(qslot, map_xq(qmaps), qbar, jj.kg * 128, jj.g, jj.t0 + kQRows * qw);
+          ptx::tma_load_3d_hint(qslot, map_xq(qmaps), qbar, jj.kg * 128, jj.g, jj.t0 + kQRows * qw,
+                                x_policy);
         }
       };
       QJob jp = j;  // L2 prefetch cursor
@@ -1316,7 +1332,11 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
           idle0 = 0;
           continue;
         }
-        if (have && q_ready()) {
+        // A job of the unit of ordinal n (this pair's n-th unit) is
+        // quantised once this warp has drained n - q_lead units: the codes
+        // then wait in L2 for a short time only, instead of being written
+        // back and read again from DRAM.
+        if (have && (j.u - u_first) / u_step <= ti + q_lead && q_ready()) {
           q_step();
           idle0 = 0;
           continue;
@@ -1894,6 +1914,15 @@ cudaError_t watchdog_read(uint32_t* value, bool clear) {
   if (e == cudaSuccess && clear) {
     const uint32_t zero = 0;
     e = cudaMemcpyToSymbol(g_watchdog, &zero, sizeof(uint32_t));
+  }
+  return e;
+}
+
+cudaError_t takeover_count(uint32_t* value, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_takeovers, sizeof(uint32_t));
+  if (e == cudaSuccess && clear) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_takeovers, &zero, sizeof(uint32_t));
   }
   return e;
 }

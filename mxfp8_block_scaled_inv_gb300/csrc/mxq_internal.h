@@ -94,6 +94,9 @@ int set_pair_limit(int pairs);
 int set_lazy_pairs(int from);
 
 cudaError_t watchdog_read(uint32_t* value, bool clear);
+// Number of prefill quantisation jobs taken over by a consumer since the
+// last clear (current device).
+cudaError_t takeover_count(uint32_t* value, bool clear);
 
 // One tiny kernel whose only wait can never be satisfied; it must give up
 // after limit_ns and set bit 31 of the watchdog word.

@@ -243,3 +243,13 @@ def test_lazy_pairs_is_a_plain_setting(L):
     assert L.mxq_debug_set_lazy_pairs(3) == -1
     assert L.mxq_debug_set_lazy_pairs(-1) == 3
     assert L.mxq_debug_set_lazy_pairs(-5) == -1
+
+
+def test_takeover_count_arguments(L):
+    assert L.mxq_debug_takeovers(None, 0) == 1  # MXQ_ERR_NULL
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_takeover_count_without_device(L):
+    v = ctypes.c_uint32(0)
+    assert L.mxq_debug_takeovers(ctypes.byref(v), 1) == 7

@@ -54,10 +54,13 @@ def run_chunk(mxq, st, chunk, T, start):
     pos = W.positions_arange(start, T)
     xd, pd = to_dev(x, pos)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mxq.mxq_debug_takeovers(clear=True)
     out = mxq.mxq_wo_a(xd, pd, st["cd"], st["sd"], st["wd"], st["wsf"], R=R, err_flag=err,
                        ws=st["ws"])
     torch.cuda.synchronize()
     assert int(err.item()) == 0
+    # With every pair resident, each quantises its own jobs in time.
+    assert mxq.mxq_debug_takeovers() == 0
     return x, pos, out
 
 

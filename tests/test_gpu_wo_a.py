@@ -269,6 +269,7 @@ def test_pair_forms_with_fewer_pairs_than_slots(mxq, pairs):
     ref = mxq.mxq_bmm_a8w8(q, sc, wd, wsf)
     torch.cuda.synchronize()
     prev = mxq.mxq_debug_set_pair_limit(pairs)
+    mxq.mxq_debug_takeovers(clear=True)
     try:
         out = mxq.mxq_wo_a(xd, pd, cd, sd, wd, wsf, R=64)
         gemm = mxq.mxq_bmm_a8w8(q, sc, wd, wsf)
@@ -277,6 +278,13 @@ def test_pair_forms_with_fewer_pairs_than_slots(mxq, pairs):
         mxq.mxq_debug_set_pair_limit(prev)
     assert torch.equal(out, ref)
     assert torch.equal(gemm, ref)
+    if pairs > 1:
+        # Every pair quantises its own jobs in time: the quantisation runs
+        # ahead of each pair's GEMM by enough units that the jobs a waiting
+        # pair needs are always allowed.  (A single pair quantises four units'
+        # jobs before its first multiply can start, which may exceed the
+        # takeover wait.)
+        assert mxq.mxq_debug_takeovers() == 0
 
 
 @pytest.mark.parametrize("lazy_from", [0, 5, 40])
@@ -299,12 +307,14 @@ def test_pair_quant_when_owners_do_not_quantise(mxq, lazy_from):
                     device="cuda")
     torch.cuda.synchronize()
     prev = mxq.mxq_debug_set_lazy_pairs(lazy_from)
+    mxq.mxq_debug_takeovers(clear=True)
     try:
         out = mxq.mxq_wo_a(xd, pd, cd, sd, wd, wsf, R=64, ws=ws)
         torch.cuda.synchronize()
     finally:
         mxq.mxq_debug_set_lazy_pairs(prev)
     assert torch.equal(out, ref)
+    assert mxq.mxq_debug_takeovers() > 0  # the takeover path ran
     assert np.array_equal(ws[:T * G * D].cpu().numpy().reshape(T, G, D), q.cpu().numpy())
 
 
