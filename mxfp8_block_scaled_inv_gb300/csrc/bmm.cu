@@ -1918,6 +1918,8 @@ cudaError_t watchdog_read(uint32_t* value, bool clear) {
   return e;
 }
 
+cudaError_t watchdog_address(uint32_t** p) { return cudaGetSymbolAddress((void**)p, g_watchdog); }
+
 cudaError_t takeover_count(uint32_t* value, bool clear) {
   cudaError_t e = cudaMemcpyFromSymbol(value, g_takeovers, sizeof(uint32_t));
   if (e == cudaSuccess && clear) {

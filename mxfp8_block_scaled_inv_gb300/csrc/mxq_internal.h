@@ -94,6 +94,9 @@ int set_pair_limit(int pairs);
 int set_lazy_pairs(int from);
 
 cudaError_t watchdog_read(uint32_t* value, bool clear);
+// Device address of the watchdog word on the current device (for kernels of
+// other translation units).
+cudaError_t watchdog_address(uint32_t** p);
 // Number of prefill quantisation jobs taken over by a consumer since the
 // last clear (current device).
 cudaError_t takeover_count(uint32_t* value, bool clear);

@@ -196,3 +196,32 @@ def test_strided_cos_sin_views(mxq):
                                           slots, np.full((ns, D), 0xA5, dtype=np.uint8), scale=0.0371)
     assert np.array_equal(W.bf16_bits(q_out.cpu()), want_q)
     assert np.array_equal(cache.cpu().numpy(), want_cache)
+
+
+@pytest.mark.parametrize("R,scale", [(64, 0.0371), (0, None), (128, 0.5)])
+def test_streaming_query_path(mxq, R, scale):
+    """Out-of-place queries of 32 MiB or more go through the streaming kernel
+    (blocks of whole rows rotated in shared memory): T = 2000 tokens of 16
+    heads x 576 (28 rows per 32 KB block, so blocks straddle tokens and the
+    last block is short), two tokens at invalid positions (their query slices
+    zero, their KV rows not written, MXQ_DEVERR_POSITION), every query bit
+    and cache byte against the oracle."""
+    T, H, D, Dk = 2000, 16, 576, 576
+    assert T * H * D * 2 >= 32 << 20 and (T * H) % 28 != 0
+    q, kv, pos, cos, sin, slots, ns = inputs(T, H, D, Dk, max(R, 16), seed=5700 + R, max_pos=4000)
+    bad = [] if R == 0 else [45, 1711]
+    if bad:
+        pos[bad] = torch.tensor([4000, -2], dtype=torch.int64)
+    q_out, cache, err, _ = run(mxq, q, kv, pos, cos, sin, R, slots, ns, scale)
+    assert err == (mxq.MXQ_DEVERR_POSITION if bad else 0)
+    good = np.array([t for t in range(T) if t not in bad])
+    g_slots = slots.copy()
+    g_slots[bad] = -1
+    want_q, want_cache = oracle(q[good], kv[good], pos[good], cos, sin, R, g_slots[good], ns, scale)
+    got_q = W.bf16_bits(q_out.cpu())
+    assert np.array_equal(got_q[good], want_q)
+    qb = W.bf16_bits(q)
+    for t in bad:
+        assert (got_q[t, :, D - R:] == 0).all()
+        assert np.array_equal(got_q[t, :, :D - R], qb[t, :, :D - R])
+    assert np.array_equal(cache_bits(cache), want_cache)
