@@ -353,10 +353,11 @@ int mxq_debug_set_lazy_pairs(int from);
 int mxq_debug_takeovers(uint32_t* host_value, int clear);
 
 /*
- * Watchdog word of the GEMM kernels on the current device (host call,
- * synchronous).  Every wait inside a kernel is bounded; a wait that runs out
- * sets a bit here and the kernel returns early instead of hanging.  0 means
- * no wait ever ran out.  With clear != 0 the word is reset after reading.
+ * Watchdog word of the GEMM kernels and of the streamed query copy of
+ * mxq_rope_kv_insert on the current device (host call, synchronous).  Every
+ * wait inside those kernels is bounded; a wait that runs out sets a bit here
+ * and the kernel returns early instead of hanging.  0 means no wait ever ran
+ * out.  With clear != 0 the word is reset after reading.
  */
 int mxq_watchdog_read(uint32_t* host_value, int clear);
 
