@@ -609,6 +609,12 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
   volatile int* act_done = &act_done_shared;
   volatile int* gate_go = gate_go_shared;
 
+  // The next kernel on the stream may be scheduled from the start: it only
+  // streams its own weights until it has waited for this grid to complete.
+  // (Triggered here rather than after this CTA's set-up: decode layers
+  // 0.9-2.9 % and the K = 576 linear 3 % faster, T = 64 and K = 288 within
+  // 1 % slower, the prefill chunk unchanged.)
+  if (threadIdx.x == 0) ptx::griddep_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // Pair form: CTAs 2i and 2i+1 share every unit; the even one issues the MMAs.
@@ -667,9 +673,6 @@ __global__ void __launch_bounds__((Cfg<SWAP, FUSED, BN, NSTAGE, PAIR, QUANT>::TH
   if constexpr (PAIR) ptx::cluster_sync();  // the peer's barriers exist before any remote arrive
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // The next kernel on the stream may be scheduled now: it only streams its
-  // own weights until it has waited for this grid to complete.
-  if (threadIdx.x == 0) ptx::griddep_launch_dependents();
 
   if (warp == 0) {
     if constexpr (FUSED) {
