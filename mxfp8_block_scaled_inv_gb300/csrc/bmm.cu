@@ -10,7 +10,10 @@
 //   A = E4M3(a) * 2^(sa-127), W = E4M3(w) * 2^(sw-127), one scale per 128 k.
 //
 // Work unit = one output tile of one group g (and, for the split-K form, one
-// K slice of it).  Warp roles (12 warps; 11 in the fused form):
+// K slice of it).  Warp roles (12 warps; 11 in the fused form; the pair
+// form adds a gate warp 12 that waits on the MMA warp's barriers, and the
+// quantising pair form, which has no scale loader, runs that gate on warp
+// 2):
 //   warp 0      weight producer: per pipeline stage (one 128-wide K group) a
 //               TMA load of the W tile (128-byte swizzle, zero fill outside
 //               the tensor: this is the unaligned-K tail) and a copy of the
